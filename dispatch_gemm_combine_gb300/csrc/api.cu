@@ -1,0 +1,503 @@
+// C ABI of the MoE expert layer: argument checks, workspace layout, TMA
+// descriptor encoding and the launch sequence of each entry point.
+//
+// Forward  (token-repeat page: repeat, masked expert FFN, weighted sum):
+//   plan -> gather X into tile-padded expert-grouped rows Xp
+//        -> gate_up GEMM, activation fused in the epilogue (A, saved H1)
+//        -> down GEMM, routing weight fused in the epilogue (Ow, reusing Xp)
+//        -> k-way combine per token (the dispatch-and-combine page's
+//           index_add_ step, in a fixed order).
+// Backward (backward page: d hidden_states, topk_weights, gate/up/down):
+//   gather dY, X -> down dgrad + activation backward (dH1, Aw, dw partials)
+//   -> dw reduce -> down wgrad -> gate_up dgrad (dXp, reusing dYp)
+//   -> combine dXp into dX -> gate_up wgrad.
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <cstring>
+#include <mutex>
+
+#include "kernels.h"
+#include "moe.h"
+
+namespace moe {
+
+cudaError_t launch_gemm_bf16_fwd(int, const CUtensorMap*, const GemmArgs&, int, cudaStream_t);
+cudaError_t launch_gemm_bf16_dgrad(int, const CUtensorMap*, const GemmArgs&, int, cudaStream_t);
+cudaError_t launch_gemm_bf16_wgrad(int, const CUtensorMap*, const GemmArgs&, int, cudaStream_t);
+cudaError_t launch_gemm_f32(int, const CUtensorMap*, const GemmArgs&, int, cudaStream_t);
+
+cudaError_t launch_gemm(int mode, int elem_bytes, const CUtensorMap* maps, const GemmArgs& args,
+                        int num_sms, cudaStream_t st) {
+  if (elem_bytes == 4) return launch_gemm_f32(mode, maps, args, num_sms, st);
+  switch (mode) {
+    case kFwdGateUp:
+    case kFwdDown: return launch_gemm_bf16_fwd(mode, maps, args, num_sms, st);
+    case kDgradDown:
+    case kDgradGateUp: return launch_gemm_bf16_dgrad(mode, maps, args, num_sms, st);
+    default: return launch_gemm_bf16_wgrad(mode, maps, args, num_sms, st);
+  }
+}
+
+int gemm_block_n(int mode, int /*elem_bytes*/) { return mode == kFwdGateUp ? 128 : 256; }
+
+}  // namespace moe
+
+using namespace moe;
+
+namespace {
+
+constexpr int kMaxExperts = 1024;
+constexpr int kMaxTopK = 32;
+std::atomic<uint64_t> g_timeout_ns{2000000000ull};
+
+// ------------------------------------------------------------ device cache
+struct DevInfo {
+  bool init = false;
+  bool supported = false;
+  int sms = 0;
+};
+std::mutex g_mu;
+DevInfo g_dev[64];
+
+moe_status device_info(int* sms) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MOE_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_mu);
+  DevInfo& d = g_dev[dev];
+  if (!d.init) {
+    int major = 0, minor = 0, n = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    d.supported = (major == 10 && minor == 3);
+    d.sms = n;
+    d.init = true;
+  }
+  if (!d.supported) return MOE_ERR_UNSUPPORTED;
+  *sms = d.sms;
+  return MOE_OK;
+}
+
+// ------------------------------------------------------------ TMA descriptors
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+CUtensorMapDataType tma_dtype(int es) {
+  return es == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+}
+
+// 2-D map over a row-major [rows, cols] view with row stride `ld` elements.
+bool map2d(CUtensorMap* m, int es, const void* base, uint64_t cols, uint64_t rows, uint64_t ld,
+           uint32_t box_c, uint32_t box_r, CUtensorMapSwizzle sw) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {ld * es};
+  cuuint32_t box[2] = {box_c, box_r};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, tma_dtype(es), 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// 3-D map over [d2, d1, d0] with strides (elements) s1 for d1 and s2 for d2.
+bool map3d(CUtensorMap* m, int es, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
+           uint64_t s1, uint64_t s2, uint32_t b0, uint32_t b1, CUtensorMapSwizzle sw) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {d0, d1, d2};
+  cuuint64_t strides[2] = {s1 * es, s2 * es};
+  cuuint32_t box[3] = {b0, b1, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return fn(m, tma_dtype(es), 3, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Output tiles of the epilogue: 32 x 32 elements, swizzled to match the
+// staging layout (64B rows for 16-bit, 128B rows for fp32).
+CUtensorMapSwizzle out_swizzle(int es) {
+  return es == 2 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B;
+}
+
+// ------------------------------------------------------------ shape & layout
+int elem_bytes(const moe_shape* s) { return s->dtype == MOE_FP32 ? 4 : 2; }
+
+bool shape_ok(const moe_shape* s) {
+  if (!s) return false;
+  if (s->T < 0 || s->H < 8 || s->I < 8 || (s->H % 8) || (s->I % 8)) return false;
+  if (s->k < 1 || s->k > kMaxTopK || s->E < s->k || s->E > kMaxExperts) return false;
+  if (s->act != MOE_ACT_SWIGLU && s->act != MOE_ACT_CLAMPED_GLU) return false;
+  if (s->dtype != MOE_BF16 && s->dtype != MOE_FP32) return false;
+  if (s->T * static_cast<int64_t>(s->k) >= (1ll << 31)) return false;
+  return true;
+}
+
+// Upper bound on the rows of the tile-padded expert-grouped layout:
+// sum_e ceil(M_e / 128) * 128 with sum M_e = Tk and at most min(E, Tk)
+// experts holding a row.
+int64_t rows_max(const moe_shape* s) {
+  const int64_t Tk = s->T * s->k;
+  const int64_t live = Tk < s->E ? Tk : s->E;
+  return (Tk + live * (kRowTile - 1)) / kRowTile * kRowTile;
+}
+
+size_t align256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
+
+struct Layout {
+  size_t err = 0, counts = 0, offsets = 0, perm = 0, inv = 0, poff = 0, blkhist = 0;
+  size_t xp = 0, act = 0, dyp = 0, dh1 = 0, aw = 0, dwpart = 0;
+  size_t total = 0;
+};
+
+int dgrad_down_ntiles(const moe_shape* s) { return (s->I + 255) / 256; }
+
+Layout layout(const moe_shape* s, int which) {
+  Layout L;
+  const int64_t Tk = s->T * s->k;
+  const int64_t R = rows_max(s);
+  const size_t es = elem_bytes(s);
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off = align256(off + bytes);
+    return o;
+  };
+  L.err = take(256);
+  L.poff = take(sizeof(int) * (s->E + 1));
+  if (which == 0 || which == 1) L.blkhist = take(sizeof(int) * plan_blkhist_ints(Tk, s->E));
+  if (which == 1) {
+    L.counts = take(sizeof(int) * s->E);
+    L.offsets = take(sizeof(int) * (s->E + 1));
+    L.perm = take(sizeof(int) * (Tk > 0 ? Tk : 1));
+    L.inv = take(sizeof(int) * (Tk > 0 ? Tk : 1));
+    L.xp = take(es * R * s->H);
+    L.act = take(es * R * s->I);
+  }
+  if (which == 2) {
+    L.dyp = take(es * R * s->H);
+    L.xp = take(es * R * s->H);
+    L.dh1 = take(es * R * 2 * s->I);
+    L.aw = take(es * R * s->I);
+    L.dwpart = take(sizeof(float) * R * dgrad_down_ntiles(s));
+  }
+  L.total = off;
+  return L;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+template <typename P>
+P* at(void* ws, size_t off) {
+  return reinterpret_cast<P*>(static_cast<char*>(ws) + off);
+}
+
+#define MOE_CUDA(x)                             \
+  do {                                          \
+    if ((x) != cudaSuccess) return MOE_ERR_CUDA; \
+  } while (0)
+
+GemmArgs base_args(const moe_shape* s, const int* poff, const int* counts, const int* offsets,
+                   const int* perm, const float* w, int* err) {
+  GemmArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.poff = poff;
+  a.counts = counts;
+  a.offsets = offsets;
+  a.perm = perm;
+  a.topk_w = w;
+  a.tk = static_cast<int>(s->T * s->k);
+  a.E = s->E;
+  a.act = s->act;
+  a.limit = s->clamp_limit;
+  a.alpha = s->alpha;
+  a.I = s->I;
+  a.rows_max = rows_max(s);
+  a.err = err;
+  a.timeout_ns = g_timeout_ns.load();
+  return a;
+}
+
+}  // namespace
+
+// ====================================================================== ABI
+extern "C" {
+
+size_t moe_workspace_size(const moe_shape* shape, int which) {
+  if (!shape_ok(shape) || which < 0 || which > 2) return 0;
+  return layout(shape, which).total;
+}
+
+size_t moe_saved_size(const moe_shape* shape) {
+  if (!shape_ok(shape)) return 0;
+  const size_t r = static_cast<size_t>(rows_max(shape));
+  return (r > 0 ? r : 1) * 2 * shape->I * elem_bytes(shape);
+}
+
+uint64_t moe_set_wait_timeout_ns(uint64_t ns) { return g_timeout_ns.exchange(ns); }
+
+const char* moe_status_string(moe_status st) {
+  switch (st) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "unsupported (needs an sm_103 GPU and a supported shape)";
+    case MOE_ERR_WORKSPACE: return "workspace too small";
+    case MOE_ERR_BAD_INDEX: return "expert index out of range";
+    case MOE_ERR_TIMEOUT: return "device pipeline wait timed out";
+    case MOE_ERR_CUDA: return "CUDA call failed";
+  }
+  return "unknown status";
+}
+
+moe_status moe_get_device_error(void* ws, moe_stream_t stream) {
+  if (!ws) return MOE_ERR_INVALID_ARG;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  MOE_CUDA(cudaStreamSynchronize(st));
+  int code = 0;
+  MOE_CUDA(cudaMemcpy(&code, ws, sizeof(int), cudaMemcpyDeviceToHost));
+  if (code != 0) MOE_CUDA(cudaMemset(ws, 0, sizeof(int)));
+  return static_cast<moe_status>(code);
+}
+
+moe_status moe_plan(const moe_shape* s, const int32_t* topk_idx, const moe_plan_t* plan, void* ws,
+                    size_t ws_bytes, moe_stream_t stream) {
+  if (!shape_ok(s) || !plan || !ws || !plan->counts || !plan->offsets) return MOE_ERR_INVALID_ARG;
+  const int64_t Tk = s->T * s->k;
+  if (Tk > 0 && (!topk_idx || !plan->perm || !plan->inv)) return MOE_ERR_INVALID_ARG;
+  const Layout L = layout(s, 0);
+  if (ws_bytes < L.total) return MOE_ERR_WORKSPACE;
+  int sms = 0;
+  const moe_status ds = device_info(&sms);
+  if (ds != MOE_OK) return ds;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  MOE_CUDA(launch_plan(topk_idx, Tk, s->E, plan->counts, plan->offsets, plan->perm, plan->inv,
+                       at<int>(ws, L.poff), at<int>(ws, L.blkhist), at<int>(ws, L.err), st));
+  return MOE_OK;
+}
+
+moe_status moe_ffn_fwd(const moe_shape* s, const void* x, const int32_t* topk_idx,
+                       const float* topk_w, const void* w_gate_up, const void* w_down,
+                       const moe_plan_t* plan, void* y, void* saved, void* ws, size_t ws_bytes,
+                       moe_stream_t stream) {
+  if (!shape_ok(s) || !ws || !w_gate_up || !w_down) return MOE_ERR_INVALID_ARG;
+  if (s->T == 0) return MOE_OK;
+  if (!x || !topk_idx || !topk_w || !y) return MOE_ERR_INVALID_ARG;
+  if (plan && (!plan->counts || !plan->offsets || !plan->perm || !plan->inv))
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(y) || !aligned16(w_gate_up) || !aligned16(w_down) ||
+      (saved && !aligned16(saved)))
+    return MOE_ERR_INVALID_ARG;
+  const Layout L = layout(s, 1);
+  if (ws_bytes < L.total) return MOE_ERR_WORKSPACE;
+  int sms = 0;
+  const moe_status ds = device_info(&sms);
+  if (ds != MOE_OK) return ds;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+
+  const int es = elem_bytes(s);
+  const int64_t Tk = s->T * s->k;
+  const int64_t R = rows_max(s);
+  const int H = s->H, I = s->I, E = s->E;
+  int* err = at<int>(ws, L.err);
+  int* poff = at<int>(ws, L.poff);
+  const int *counts, *offsets, *perm, *inv;
+  if (plan) {
+    counts = plan->counts;
+    offsets = plan->offsets;
+    perm = plan->perm;
+    inv = plan->inv;
+    MOE_CUDA(launch_padded_offsets(counts, E, poff, st));
+  } else {
+    int* c = at<int>(ws, L.counts);
+    int* o = at<int>(ws, L.offsets);
+    int* p = at<int>(ws, L.perm);
+    int* v = at<int>(ws, L.inv);
+    MOE_CUDA(launch_plan(topk_idx, Tk, E, c, o, p, v, poff, at<int>(ws, L.blkhist), err, st));
+    counts = c;
+    offsets = o;
+    perm = p;
+    inv = v;
+  }
+  void* xp = at<char>(ws, L.xp);
+  void* aact = at<char>(ws, L.act);
+  MOE_CUDA(launch_gather_rows(x, H, s->k, E, poff, counts, offsets, perm, static_cast<int>(Tk), R, xp,
+                              es, sms, st));
+
+  const uint32_t BK = 128 / es, CH = 128 / es;
+  const auto SW = CU_TENSOR_MAP_SWIZZLE_128B;
+  const auto OSW = out_swizzle(es);
+  const char* wgu = static_cast<const char*>(w_gate_up);
+
+  // gate_up GEMM + activation
+  CUtensorMap m1[6];
+  bool ok = map2d(&m1[0], es, xp, H, R, H, BK, 128, SW) &&
+            map3d(&m1[1], es, wgu, I, H, E, 2ll * I, 2ll * I * H, CH, BK, SW) &&
+            map3d(&m1[2], es, wgu + static_cast<size_t>(I) * es, I, H, E, 2ll * I, 2ll * I * H,
+                  CH, BK, SW) &&
+            map2d(&m1[3], es, aact, I, R, I, 32, 32, OSW);
+  if (ok && saved) {
+    ok = map2d(&m1[4], es, saved, I, R, 2ll * I, 32, 32, OSW) &&
+         map2d(&m1[5], es, static_cast<char*>(saved) + static_cast<size_t>(I) * es, I, R, 2ll * I,
+               32, 32, OSW);
+  } else {
+    m1[4] = m1[3];
+    m1[5] = m1[3];
+  }
+  if (!ok) return MOE_ERR_CUDA;
+  GemmArgs a1 = base_args(s, poff, counts, offsets, perm, topk_w, err);
+  a1.num_kb = (H + BK - 1) / BK;
+  a1.n_tiles = (I + gemm_block_n(kFwdGateUp, es) - 1) / gemm_block_n(kFwdGateUp, es);
+  a1.save_h1 = saved ? 1 : 0;
+  MOE_CUDA(launch_gemm(kFwdGateUp, es, m1, a1, sms, st));
+
+  // down GEMM * routing weight -> Ow (reuses the Xp buffer)
+  void* ow = xp;
+  CUtensorMap m2[6];
+  ok = map2d(&m2[0], es, aact, I, R, I, BK, 128, SW) &&
+       map3d(&m2[1], es, w_down, H, I, E, H, static_cast<int64_t>(H) * I, CH, BK, SW) &&
+       map2d(&m2[3], es, ow, H, R, H, 32, 32, OSW);
+  if (!ok) return MOE_ERR_CUDA;
+  m2[2] = m2[1];
+  m2[4] = m2[3];
+  m2[5] = m2[3];
+  GemmArgs a2 = base_args(s, poff, counts, offsets, perm, topk_w, err);
+  a2.num_kb = (I + BK - 1) / BK;
+  a2.n_tiles = (H + gemm_block_n(kFwdDown, es) - 1) / gemm_block_n(kFwdDown, es);
+  MOE_CUDA(launch_gemm(kFwdDown, es, m2, a2, sms, st));
+
+  // combine
+  MOE_CUDA(launch_combine(ow, H, s->k, E, topk_idx, inv, offsets, poff, s->T, R, y, es, sms, st));
+  return MOE_OK;
+}
+
+moe_status moe_ffn_bwd(const moe_shape* s, const void* dy, const void* x, const int32_t* topk_idx,
+                       const float* topk_w, const void* w_gate_up, const void* w_down,
+                       const moe_plan_t* plan, const void* saved, void* dx, float* d_topk_w,
+                       float* dw_gate_up, float* dw_down, void* ws, size_t ws_bytes,
+                       moe_stream_t stream) {
+  if (!shape_ok(s) || !ws || !w_gate_up || !w_down || !dw_gate_up || !dw_down)
+    return MOE_ERR_INVALID_ARG;
+  int sms = 0;
+  const moe_status ds = device_info(&sms);
+  if (ds != MOE_OK) return ds;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const int es = elem_bytes(s);
+  const int H = s->H, I = s->I, E = s->E;
+  if (s->T == 0) {
+    MOE_CUDA(cudaMemsetAsync(dw_gate_up, 0, sizeof(float) * E * H * 2ull * I, st));
+    MOE_CUDA(cudaMemsetAsync(dw_down, 0, sizeof(float) * E * static_cast<size_t>(I) * H, st));
+    return MOE_OK;
+  }
+  if (!dy || !x || !topk_idx || !topk_w || !plan || !saved || !dx || !d_topk_w)
+    return MOE_ERR_INVALID_ARG;
+  if (!plan->counts || !plan->offsets || !plan->perm || !plan->inv) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(dy) || !aligned16(x) || !aligned16(dx) || !aligned16(saved) ||
+      !aligned16(w_gate_up) || !aligned16(w_down) || !aligned16(dw_gate_up) ||
+      !aligned16(dw_down))
+    return MOE_ERR_INVALID_ARG;
+  const Layout L = layout(s, 2);
+  if (ws_bytes < L.total) return MOE_ERR_WORKSPACE;
+
+  const int64_t Tk = s->T * s->k;
+  const int64_t R = rows_max(s);
+  int* err = at<int>(ws, L.err);
+  int* poff = at<int>(ws, L.poff);
+  const int* counts = plan->counts;
+  const int* offsets = plan->offsets;
+  const int* perm = plan->perm;
+  const int* inv = plan->inv;
+  MOE_CUDA(launch_padded_offsets(counts, E, poff, st));
+
+  void* dyp = at<char>(ws, L.dyp);
+  void* xp = at<char>(ws, L.xp);
+  void* dh1 = at<char>(ws, L.dh1);
+  void* aw = at<char>(ws, L.aw);
+  float* dwpart = at<float>(ws, L.dwpart);
+  MOE_CUDA(launch_gather_rows(dy, H, s->k, E, poff, counts, offsets, perm, static_cast<int>(Tk), R,
+                              dyp, es, sms, st));
+  MOE_CUDA(launch_gather_rows(x, H, s->k, E, poff, counts, offsets, perm, static_cast<int>(Tk), R, xp,
+                              es, sms, st));
+
+  const uint32_t BK = 128 / es, CH = 128 / es;
+  const auto SW = CU_TENSOR_MAP_SWIZZLE_128B;
+  const auto OSW = out_swizzle(es);
+  const auto OSW32 = out_swizzle(4);
+  const char* dh1c = static_cast<const char*>(dh1);
+  bool ok;
+
+  // (1) down dgrad + activation backward -> dH1 (gate | up), Aw, dw partials
+  CUtensorMap m1[6];
+  ok = map2d(&m1[0], es, dyp, H, R, H, BK, 128, SW) &&
+       map3d(&m1[1], es, w_down, H, I, E, H, static_cast<int64_t>(H) * I, BK, 256, SW) &&
+       map2d(&m1[3], es, dh1, I, R, 2ll * I, 32, 32, OSW) &&
+       map2d(&m1[4], es, dh1c + static_cast<size_t>(I) * es, I, R, 2ll * I, 32, 32, OSW) &&
+       map2d(&m1[5], es, aw, I, R, I, 32, 32, OSW);
+  if (!ok) return MOE_ERR_CUDA;
+  m1[2] = m1[1];
+  GemmArgs a1 = base_args(s, poff, counts, offsets, perm, topk_w, err);
+  a1.num_kb = (H + BK - 1) / BK;
+  a1.n_tiles = dgrad_down_ntiles(s);
+  a1.h1 = saved;
+  a1.dwpart = dwpart;
+  MOE_CUDA(launch_gemm(kDgradDown, es, m1, a1, sms, st));
+  MOE_CUDA(launch_dw_reduce(dwpart, a1.n_tiles, R, E, topk_idx, inv, offsets, poff, Tk, d_topk_w, st));
+
+  // (2) down wgrad: dWd[e] = Aw_e^T dYp_e
+  CUtensorMap m2[6];
+  ok = map2d(&m2[0], es, aw, I, R, I, CH, BK, SW) && map2d(&m2[1], es, dyp, H, R, H, CH, BK, SW) &&
+       map3d(&m2[3], 4, dw_down, H, I, E, H, static_cast<int64_t>(H) * I, 32, 32, OSW32);
+  if (!ok) return MOE_ERR_CUDA;
+  m2[2] = m2[1];
+  m2[4] = m2[3];
+  m2[5] = m2[3];
+  GemmArgs a2 = base_args(s, poff, counts, offsets, perm, topk_w, err);
+  a2.m_tiles = (I + 127) / 128;
+  a2.n_tiles = (H + 255) / 256;
+  MOE_CUDA(launch_gemm(kWgradDown, es, m2, a2, sms, st));
+
+  // (3) gate_up dgrad: dXp = dH1 Wgu[e]^T  (written over dYp)
+  void* dxp = dyp;
+  CUtensorMap m3[6];
+  ok = map2d(&m3[0], es, dh1, 2ll * I, R, 2ll * I, BK, 128, SW) &&
+       map3d(&m3[1], es, w_gate_up, 2ll * I, H, E, 2ll * I, 2ll * I * H, BK, 256, SW) &&
+       map2d(&m3[3], es, dxp, H, R, H, 32, 32, OSW);
+  if (!ok) return MOE_ERR_CUDA;
+  m3[2] = m3[1];
+  m3[4] = m3[3];
+  m3[5] = m3[3];
+  GemmArgs a3 = base_args(s, poff, counts, offsets, perm, topk_w, err);
+  a3.num_kb = (2 * I + BK - 1) / BK;
+  a3.n_tiles = (H + 255) / 256;
+  MOE_CUDA(launch_gemm(kDgradGateUp, es, m3, a3, sms, st));
+  MOE_CUDA(launch_combine(dxp, H, s->k, E, topk_idx, inv, offsets, poff, s->T, R, dx, es, sms, st));
+
+  // (4) gate_up wgrad: dWgu[e] = Xp_e^T dH1_e
+  CUtensorMap m4[6];
+  ok = map2d(&m4[0], es, xp, H, R, H, CH, BK, SW) &&
+       map2d(&m4[1], es, dh1, 2ll * I, R, 2ll * I, CH, BK, SW) &&
+       map3d(&m4[3], 4, dw_gate_up, 2ll * I, H, E, 2ll * I, 2ll * I * H, 32, 32, OSW32);
+  if (!ok) return MOE_ERR_CUDA;
+  m4[2] = m4[1];
+  m4[4] = m4[3];
+  m4[5] = m4[3];
+  GemmArgs a4 = base_args(s, poff, counts, offsets, perm, topk_w, err);
+  a4.m_tiles = (H + 127) / 128;
+  a4.n_tiles = (2 * I + 255) / 256;
+  MOE_CUDA(launch_gemm(kWgradGateUp, es, m4, a4, sms, st));
+  return MOE_OK;
+}
+
+}  // extern "C"

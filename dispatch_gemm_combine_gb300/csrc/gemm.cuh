@@ -1,0 +1,553 @@
+// Grouped (per-expert) GEMM on the sm_103a tensor cores: TMA loads into a
+// multi-stage shared-memory ring, tcgen05.mma issued by one thread with the
+// fp32 accumulator in tensor memory (double-buffered), and a 4-warp epilogue
+// that reads the accumulator with tcgen05.ld, applies the mode's fused
+// elementwise work and writes 32x32 output tiles with TMA stores.
+//
+// One persistent CTA per SM walks a static tile sequence (CTA b takes tiles
+// b, b + grid, ...).  Warp roles: warp 0 = TMA producer, warp 1 = MMA issuer
+// (and tensor-memory owner), warps 2..5 = epilogue (warp w reads TMEM lanes
+// 32*(w%4) .. 32*(w%4)+31, i.e. tile rows).
+//
+// Row-grouped modes (forward and dgrad) tile the tile-padded expert-grouped
+// row space: expert e owns rows [poff[e], poff[e+1]), a multiple of 128, so
+// no M tile straddles two experts.  Tiles are ordered (expert, n, m) so the
+// CTAs running at the same time share one expert's weight columns in L2.
+// Weight-gradient modes tile the [E, M, N] output and contract over the
+// expert's padded rows (zero-filled padding contributes nothing).
+//
+// Operand layouts (smem, 128-byte swizzle, what TMA writes):
+//   K-major   box {128 B of K, rows}: 8-row groups 1024 B apart (SBO); the
+//             k-th MMA of a block starts 32*k bytes in.
+//   MN-major  boxes {128 B of M or N, BK rows of K}, one per 128 B of M/N,
+//             BK*128 B apart (LBO); 8-row K groups 1024 B apart (SBO); the
+//             k-th MMA starts k * (MMA K rows) * 128 bytes in.
+#pragma once
+
+#include "kernels.h"
+
+namespace moe {
+
+// Limit on the waits that drain copies and MMAs already in flight when a CTA
+// unwinds after a timeout; independent of the (adjustable) pipeline limit so
+// that a CTA never exits with asynchronous work still writing its memory.
+constexpr uint64_t kDrainNs = 1000000000ull;
+
+template <typename T, int MODE, int BN, int STAGES, int NBUF>
+struct GemmCfg {
+  static constexpr int kES = sizeof(T);
+  static constexpr bool kTf32 = (kES == 4);
+  static constexpr int BM = 128;
+  static constexpr int BK = 128 / kES;           // elements in one 128-byte row
+  static constexpr int CH = 128 / kES;           // MN-major chunk width (elements)
+  static constexpr int MMA_K = 32 / kES;         // K of one tcgen05.mma
+  static constexpr int KSTEPS = BK / MMA_K;      // MMAs per k-block (4)
+  static constexpr bool kWgrad = (MODE == kWgradDown || MODE == kWgradGateUp);
+  static constexpr bool A_MN = kWgrad;
+  static constexpr bool B_MN = (MODE == kFwdGateUp || MODE == kFwdDown || kWgrad);
+  static constexpr int A_BYTES = BM * 128;
+  static constexpr int B_BYTES = BN * 128;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int CHUNK_BYTES = BK * 128;   // one MN-major box
+  // output element size of the epilogue tiles
+  static constexpr int OUT_ES = kWgrad ? 4 : kES;
+  static constexpr int OUT_TILE = 32 * 32 * OUT_ES;
+  static constexpr int EPI_BYTES = 4 * NBUF * OUT_TILE;
+  static constexpr int BAR_BYTES = (2 * STAGES + 5) * 8 + 16;
+  static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + EPI_BYTES + BAR_BYTES;
+  static constexpr int TMEM_COLS = (2 * BN <= 256) ? 256 : 512;
+  // output columns produced per tile (gate_up: BN/2 gate + BN/2 up -> BN/2)
+  static constexpr int BN_OUT = (MODE == kFwdGateUp) ? BN / 2 : BN;
+  static constexpr uint32_t IDESC = make_idesc(kTf32, A_MN, B_MN, BM, BN);
+  static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+  static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "BN");
+  static_assert(!B_MN || BN % CH == 0, "MN-major B needs whole chunks");
+};
+
+struct TileInfo {
+  int e;       // expert
+  int row0;    // row-grouped: first padded row; wgrad: first padded row of expert
+  int n0;      // first output column
+  int m0;      // wgrad: first output row
+  int nkb;     // k-blocks
+  int nt;      // column-tile index
+};
+
+template <int BN_OUT, bool kWgrad>
+__device__ __forceinline__ TileInfo decode_tile(const GemmArgs& a, int t, int bk) {
+  TileInfo ti;
+  if constexpr (kWgrad) {
+    const int per_e = a.m_tiles * a.n_tiles;
+    ti.e = t / per_e;
+    const int r = t - ti.e * per_e;
+    const int m = r / a.n_tiles;
+    ti.nt = r - m * a.n_tiles;
+    ti.m0 = m * 128;
+    ti.n0 = ti.nt * BN_OUT;
+    ti.row0 = __ldg(a.poff + ti.e);
+    ti.nkb = (__ldg(a.poff + ti.e + 1) - ti.row0) / bk;
+  } else {
+    const int NT = a.n_tiles;
+    int lo = 0, hi = a.E - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if ((__ldg(a.poff + mid) >> 7) * NT <= t)
+        lo = mid;
+      else
+        hi = mid - 1;
+    }
+    ti.e = lo;
+    const int p0 = __ldg(a.poff + lo);
+    const int mt = (__ldg(a.poff + lo + 1) - p0) >> 7;
+    const int local = t - (p0 >> 7) * NT;
+    const int n = local / mt;
+    const int m = local - n * mt;
+    ti.nt = n;
+    ti.row0 = p0 + m * 128;
+    ti.n0 = n * BN_OUT;
+    ti.m0 = 0;
+    ti.nkb = a.num_kb;
+  }
+  return ti;
+}
+
+template <typename T>
+__device__ __forceinline__ float act_fwd(int act, float g, float u, float L, float alpha) {
+  if (act == 0) return g * sigmoidf_(g) * u;
+  const float gc = fminf(g, L);
+  const float uc = fminf(fmaxf(u, -L), L);
+  return (uc + 1.f) * gc * sigmoidf_(alpha * gc);
+}
+
+// a, da/dg, da/du (inclusive clamp masks)
+__device__ __forceinline__ void act_bwd(int act, float g, float u, float L, float alpha, float& a,
+                                        float& dg, float& du) {
+  if (act == 0) {
+    const float s = sigmoidf_(g);
+    const float sg = g * s;
+    a = sg * u;
+    dg = u * s * (1.f + g * (1.f - s));
+    du = sg;
+  } else {
+    const float gc = fminf(g, L);
+    const float uc = fminf(fmaxf(u, -L), L);
+    const float s = sigmoidf_(alpha * gc);
+    const float glu = gc * s;
+    a = (uc + 1.f) * glu;
+    dg = (g <= L) ? (uc + 1.f) * (s + alpha * gc * s * (1.f - s)) : 0.f;
+    du = (u >= -L && u <= L) ? glu : 0.f;
+  }
+}
+
+// Write 32 values (this thread's row of a 32x32 output tile) into a staging
+// tile in the swizzled layout the TMA store expects: 64-byte rows with the
+// 64B swizzle for 16-bit outputs, 128-byte rows with the 128B swizzle for
+// fp32 outputs.  The 16-byte unit j of row r sits at unit j ^ f(r), so the
+// 32 lanes of a warp (one row each) spread over all banks.
+template <typename O>
+__device__ __forceinline__ void stage_row(uint8_t* buf, int lane, const float (&v)[32]) {
+  if constexpr (sizeof(O) == 2) {
+    uint8_t* row = buf + lane * 64;
+    const int x = (lane >> 1) & 3;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      uint4 pk;
+      __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&pk);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) h[i] = __floats2bfloat162_rn(v[8 * j + 2 * i], v[8 * j + 2 * i + 1]);
+      *reinterpret_cast<uint4*>(row + ((j ^ x) << 4)) = pk;
+    }
+  } else {
+    uint8_t* row = buf + lane * 128;
+    const int x = lane & 7;
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      *reinterpret_cast<uint4*>(row + ((j ^ x) << 4)) =
+          make_uint4(__float_as_uint(v[4 * j]), __float_as_uint(v[4 * j + 1]),
+                     __float_as_uint(v[4 * j + 2]), __float_as_uint(v[4 * j + 3]));
+  }
+}
+
+template <typename T, int MODE, int BN, int STAGES, int NBUF>
+__global__ void __launch_bounds__(192, 1)
+    moe_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
+                    const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmO0,
+                    const __grid_constant__ CUtensorMap tmO1, const __grid_constant__ CUtensorMap tmO2,
+                    const GemmArgs args) {
+  using C = GemmCfg<T, MODE, BN, STAGES, NBUF>;
+  using OutT = typename std::conditional<C::kWgrad, float, T>::type;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t sbase = (raw + 1023u) & ~1023u;
+  uint8_t* gbase = smem_raw + (sbase - raw);
+  const uint32_t s_stages = sbase;
+  uint8_t* epi_g = gbase + STAGES * C::STAGE_BYTES;
+  const uint32_t bars = sbase + STAGES * C::STAGE_BYTES + C::EPI_BYTES;
+  const uint32_t full_bar = bars;                    // [STAGES]
+  const uint32_t empty_bar = bars + 8 * STAGES;      // [STAGES]
+  const uint32_t tfull_bar = bars + 16 * STAGES;     // [2]
+  const uint32_t tempty_bar = tfull_bar + 16;        // [2]
+  const uint32_t drain_bar = tempty_bar + 16;        // [1] error path only
+  const uint32_t tmem_slot = drain_bar + 8;
+  volatile uint32_t* tmem_slot_g =
+      reinterpret_cast<volatile uint32_t*>(gbase + (tmem_slot - sbase));
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (warp == 0 && lane == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full_bar + 8 * s, 1);
+      mbar_init(empty_bar + 8 * s, 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(tfull_bar + 8 * s, 1);
+      mbar_init(tempty_bar + 8 * s, 128);
+    }
+    mbar_init(drain_bar, 1);
+    fence_barrier_init();
+    prefetch_tmap(&tmA);
+    prefetch_tmap(&tmB0);
+    prefetch_tmap(&tmB1);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot_g;
+
+  int total;
+  if constexpr (C::kWgrad)
+    total = args.E * args.m_tiles * args.n_tiles;
+  else
+    total = static_cast<int>(min(static_cast<int64_t>(__ldg(args.poff + args.E)), args.rows_max) >> 7) *
+            args.n_tiles;
+
+  const uint64_t tmo = args.timeout_ns;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    int stage = 0;
+    uint32_t phase = 0;
+    int64_t issued = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+      const TileInfo ti = decode_tile<C::BN_OUT, C::kWgrad>(args, t, C::BK);
+      for (int kb = 0; kb < ti.nkb; ++kb) {
+        int good = 1;
+        if (lane == 0) good = mbar_wait(empty_bar + 8 * stage, phase ^ 1u, tmo);
+        good = __shfl_sync(0xffffffffu, good, 0);
+        if (!good) {
+          if (lane == 0) record_error(args.err, kErrTimeout);
+          ok = false;
+          break;
+        }
+        if (lane == 0) {
+          const uint32_t fb = full_bar + 8 * stage;
+          const uint32_t sA = s_stages + stage * C::STAGE_BYTES;
+          const uint32_t sB = sA + C::A_BYTES;
+          mbar_arrive_expect_tx(fb, C::STAGE_BYTES);
+          const int kc = kb * C::BK;
+          if constexpr (MODE == kFwdGateUp) {
+            tma_load_2d(sA, &tmA, fb, kc, ti.row0);
+            constexpr int HALF_CH = (BN / 2) / C::CH;
+#pragma unroll
+            for (int c = 0; c < HALF_CH; ++c) {
+              tma_load_3d(sB + c * C::CHUNK_BYTES, &tmB0, fb, ti.n0 + c * C::CH, kc, ti.e);
+              tma_load_3d(sB + (HALF_CH + c) * C::CHUNK_BYTES, &tmB1, fb, ti.n0 + c * C::CH, kc,
+                          ti.e);
+            }
+          } else if constexpr (MODE == kFwdDown) {
+            tma_load_2d(sA, &tmA, fb, kc, ti.row0);
+#pragma unroll
+            for (int c = 0; c < BN / C::CH; ++c)
+              tma_load_3d(sB + c * C::CHUNK_BYTES, &tmB0, fb, ti.n0 + c * C::CH, kc, ti.e);
+          } else if constexpr (MODE == kDgradDown || MODE == kDgradGateUp) {
+            tma_load_2d(sA, &tmA, fb, kc, ti.row0);
+            tma_load_3d(sB, &tmB0, fb, kc, ti.n0, ti.e);
+          } else {
+            const int r = ti.row0 + kc;
+#pragma unroll
+            for (int c = 0; c < 128 / C::CH; ++c)
+              tma_load_2d(sA + c * C::CHUNK_BYTES, &tmA, fb, ti.m0 + c * C::CH, r);
+#pragma unroll
+            for (int c = 0; c < BN / C::CH; ++c)
+              tma_load_2d(sB + c * C::CHUNK_BYTES, &tmB0, fb, ti.n0 + c * C::CH, r);
+          }
+        }
+        __syncwarp();
+        ++issued;
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+    // Before the CTA may exit, every load issued must have landed.
+    if (lane == 0) {
+      for (int s = 0; s < STAGES; ++s) {
+        const int64_t n_s = (issued > s) ? (issued - 1 - s) / STAGES + 1 : 0;
+        if (n_s > 0 &&
+            !mbar_wait(full_bar + 8 * s, static_cast<uint32_t>((n_s - 1) & 1), kDrainNs))
+          record_error(args.err, kErrTimeout);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    int stage = 0;
+    uint32_t phase = 0;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+      const TileInfo ti = decode_tile<C::BN_OUT, C::kWgrad>(args, t, C::BK);
+      int good = 1;
+      if (lane == 0) good = mbar_wait(tempty_bar + 8 * acc, acc_phase ^ 1u, tmo);
+      good = __shfl_sync(0xffffffffu, good, 0);
+      if (!good) {
+        if (lane == 0) record_error(args.err, kErrTimeout);
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t d_tmem = tmem_base + acc * BN;
+      for (int kb = 0; kb < ti.nkb; ++kb) {
+        if (lane == 0) good = mbar_wait(full_bar + 8 * stage, phase, tmo);
+        good = __shfl_sync(0xffffffffu, good, 0);
+        if (!good) {
+          if (lane == 0) record_error(args.err, kErrTimeout);
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        if (lane == 0) {
+          const uint32_t sA = s_stages + stage * C::STAGE_BYTES;
+          const uint32_t sB = sA + C::A_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < C::KSTEPS; ++kk) {
+            uint64_t adesc, bdesc;
+            if constexpr (C::A_MN)
+              adesc = smem_desc_sw128(sA + kk * C::MMA_K * 128, C::CHUNK_BYTES, 1024);
+            else
+              adesc = smem_desc_sw128(sA + kk * 32, 16, 1024);
+            if constexpr (C::B_MN)
+              bdesc = smem_desc_sw128(sB + kk * C::MMA_K * 128, C::CHUNK_BYTES, 1024);
+            else
+              bdesc = smem_desc_sw128(sB + kk * 32, 16, 1024);
+            tc_mma<C::kTf32>(d_tmem, adesc, bdesc, C::IDESC, (kb | kk) != 0 ? 1u : 0u);
+          }
+          tc_commit(empty_bar + 8 * stage);
+        }
+        __syncwarp();
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      if (!ok) break;
+      if (lane == 0) {
+        if (ti.nkb > 0)
+          tc_commit(tfull_bar + 8 * acc);
+        else
+          mbar_arrive(tfull_bar + 8 * acc);
+      }
+      __syncwarp();
+      if (++acc == 2) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    }
+    if (!ok) {
+      // Unwinding after a timeout: let the MMAs already issued finish before
+      // tensor memory is released.
+      if (lane == 0) {
+        tc_commit(drain_bar);
+        if (!mbar_wait(drain_bar, 0, kDrainNs)) record_error(args.err, kErrTimeout);
+      }
+      __syncwarp();
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;                 // TMEM lane quarter = tile rows q*32..q*32+31
+    uint8_t* my_epi = epi_g + (warp - 2) * NBUF * C::OUT_TILE;
+    const uint32_t my_epi_s = smem_u32(my_epi);
+    int buf = 0;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+
+    // stage `v` as this warp's 32x32 tile and store it with TMA at (c0, c1[, c2])
+    auto emit = [&](const CUtensorMap* map, const float (&v)[32], int c0, int c1, int c2,
+                    bool three_d) {
+      if (lane == 0) bulk_wait_read<NBUF - 1>();
+      __syncwarp();
+      uint8_t* b = my_epi + buf * C::OUT_TILE;
+      stage_row<OutT>(b, lane, v);
+      fence_async_shared();
+      __syncwarp();
+      if (lane == 0) {
+        const uint32_t bs = my_epi_s + buf * C::OUT_TILE;
+        if (three_d)
+          tma_store_3d(map, bs, c0, c1, c2);
+        else
+          tma_store_2d(map, bs, c0, c1);
+        bulk_commit();
+      }
+      __syncwarp();
+      if (++buf == NBUF) buf = 0;
+    };
+
+    for (int t = blockIdx.x; t < total; t += gridDim.x) {
+      const TileInfo ti = decode_tile<C::BN_OUT, C::kWgrad>(args, t, C::BK);
+      int good = 1;
+      if (lane == 0) good = mbar_wait(tfull_bar + 8 * acc, acc_phase, tmo);
+      good = __shfl_sync(0xffffffffu, good, 0);
+      if (!good) {
+        if (lane == 0) record_error(args.err, kErrTimeout);
+        break;
+      }
+      tc_fence_after();
+      const uint32_t tacc = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
+      const int row = ti.row0 + q * 32 + lane;   // row-grouped modes: padded row of this thread
+      float v[32];
+
+      if constexpr (C::kWgrad) {
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          if (ti.nkb > 0) {
+            tmem_ld32(tacc + c * 32, v);
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = 0.f;
+          }
+          emit(&tmO0, v, ti.n0 + c * 32, ti.m0 + q * 32, ti.e, true);
+        }
+      } else {
+        // routing weight and liveness of this thread's row
+        const int local = row - __ldg(args.poff + ti.e);
+        const bool live = local < __ldg(args.counts + ti.e);
+        float wrow = 0.f;
+        if constexpr (MODE == kFwdDown || MODE == kDgradDown) {
+          const int gi = __ldg(args.offsets + ti.e) + local;
+          if (live && gi < args.tk) {
+            const int slot = __ldg(args.perm + gi);
+            if (slot >= 0 && slot < args.tk) wrow = __ldg(args.topk_w + slot);
+          }
+        }
+        if constexpr (MODE == kFwdGateUp) {
+#pragma unroll 1
+          for (int c = 0; c < BN / 64; ++c) {
+            float u[32];
+            tmem_ld32(tacc + c * 32, v);
+            tmem_ld32(tacc + BN / 2 + c * 32, u);
+            if (args.save_h1) {
+              emit(&tmO1, v, ti.n0 + c * 32, ti.row0 + q * 32, 0, false);
+              emit(&tmO2, u, ti.n0 + c * 32, ti.row0 + q * 32, 0, false);
+            }
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = act_fwd<T>(args.act, v[i], u[i], args.limit, args.alpha);
+            emit(&tmO0, v, ti.n0 + c * 32, ti.row0 + q * 32, 0, false);
+          }
+        } else if constexpr (MODE == kFwdDown) {
+#pragma unroll 1
+          for (int c = 0; c < BN / 32; ++c) {
+            tmem_ld32(tacc + c * 32, v);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] *= wrow;
+            emit(&tmO0, v, ti.n0 + c * 32, ti.row0 + q * 32, 0, false);
+          }
+        } else if constexpr (MODE == kDgradGateUp) {
+#pragma unroll 1
+          for (int c = 0; c < BN / 32; ++c) {
+            tmem_ld32(tacc + c * 32, v);
+            emit(&tmO0, v, ti.n0 + c * 32, ti.row0 + q * 32, 0, false);
+          }
+        } else {  // kDgradDown
+          const T* h1row = static_cast<const T*>(args.h1) + static_cast<int64_t>(row) * 2 * args.I;
+          float dot = 0.f;
+#pragma unroll 1
+          for (int c = 0; c < BN / 32; ++c) {
+            tmem_ld32(tacc + c * 32, v);   // dA' (before the routing weight)
+            const int i0 = ti.n0 + c * 32;
+            float g[32], u[32];
+            if (i0 + 32 <= args.I) {
+              const uint4* gp = reinterpret_cast<const uint4*>(h1row + i0);
+              const uint4* up = reinterpret_cast<const uint4*>(h1row + args.I + i0);
+              constexpr int NV = 32 * sizeof(T) / 16;
+#pragma unroll
+              for (int j = 0; j < NV; ++j) {
+                const uint4 gv = __ldg(gp + j);
+                const uint4 uv = __ldg(up + j);
+                const T* gt = reinterpret_cast<const T*>(&gv);
+                const T* ut = reinterpret_cast<const T*>(&uv);
+#pragma unroll
+                for (int i = 0; i < 16 / static_cast<int>(sizeof(T)); ++i) {
+                  g[j * (16 / sizeof(T)) + i] = to_f32(gt[i]);
+                  u[j * (16 / sizeof(T)) + i] = to_f32(ut[i]);
+                }
+              }
+            } else {
+#pragma unroll
+              for (int i = 0; i < 32; ++i) {
+                const bool in = (i0 + i) < args.I;
+                g[i] = in ? to_f32(h1row[i0 + i]) : 0.f;
+                u[i] = in ? to_f32(h1row[args.I + i0 + i]) : 0.f;
+              }
+            }
+            float dg[32], du[32], aw[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              float a, pg, pu;
+              act_bwd(args.act, g[i], u[i], args.limit, args.alpha, a, pg, pu);
+              dot += v[i] * a;
+              const float da = wrow * v[i];
+              dg[i] = da * pg;
+              du[i] = da * pu;
+              aw[i] = wrow * a;
+            }
+            emit(&tmO0, dg, i0, ti.row0 + q * 32, 0, false);
+            emit(&tmO1, du, i0, ti.row0 + q * 32, 0, false);
+            emit(&tmO2, aw, i0, ti.row0 + q * 32, 0, false);
+          }
+          args.dwpart[static_cast<int64_t>(ti.nt) * args.rows_max + row] = live ? dot : 0.f;
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(tempty_bar + 8 * acc);
+      if (++acc == 2) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    }
+    if (lane == 0) bulk_wait_all();
+    __syncwarp();
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem_base, C::TMEM_COLS);
+}
+
+template <typename T, int MODE, int BN, int STAGES, int NBUF>
+cudaError_t launch_gemm_t(const CUtensorMap* maps, const GemmArgs& args, int num_sms,
+                          cudaStream_t st) {
+  using C = GemmCfg<T, MODE, BN, STAGES, NBUF>;
+  auto kern = moe_gemm_kernel<T, MODE, BN, STAGES, NBUF>;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  static bool configured[64] = {};
+  if (dev < 64 && !configured[dev]) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    configured[dev] = true;
+  }
+  kern<<<num_sms, 192, C::SMEM_BYTES, st>>>(maps[0], maps[1], maps[2], maps[3], maps[4], maps[5],
+                                            args);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

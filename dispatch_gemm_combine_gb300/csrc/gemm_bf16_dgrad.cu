@@ -1,0 +1,17 @@
+// bf16 backward data-gradient grouped GEMMs: down dgrad + activation
+// backward + d(topk weights) partials, gate_up dgrad.
+#include "gemm.cuh"
+
+namespace moe {
+
+cudaError_t launch_gemm_bf16_dgrad(int mode, const CUtensorMap* maps, const GemmArgs& a, int sms,
+                                   cudaStream_t st) {
+  using T = __nv_bfloat16;
+  switch (mode) {
+    case kDgradDown: return launch_gemm_t<T, kDgradDown, 256, 4, 3>(maps, a, sms, st);
+    case kDgradGateUp: return launch_gemm_t<T, kDgradGateUp, 256, 4, 2>(maps, a, sms, st);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace moe

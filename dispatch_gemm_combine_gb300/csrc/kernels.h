@@ -1,0 +1,77 @@
+// Internal launchers of the sm_103a kernels (not part of the C ABI).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "common.cuh"
+
+namespace moe {
+
+// ---- dispatch plan (plan.cu)
+cudaError_t launch_plan(const int* idx, int64_t Tk, int E, int* counts, int* offsets, int* perm,
+                        int* inv, int* poff, int* blkhist, int* err, cudaStream_t st);
+cudaError_t launch_padded_offsets(const int* counts, int E, int* poff, cudaStream_t st);
+size_t plan_blkhist_ints(int64_t Tk, int E);
+
+// ---- row movement (permute.cu); elem_bytes is 2 (bf16) or 4 (fp32)
+// dst[p] = src[perm[offsets[e] + p - poff[e]] / k] for the live rows of the
+// tile-padded expert-grouped layout; padding rows (and rows whose slot is
+// outside [0, tk)) are zero-filled.
+cudaError_t launch_gather_rows(const void* src, int H, int k, int E, const int* poff,
+                               const int* counts, const int* offsets, const int* perm, int tk,
+                               int64_t rows_max, void* dst, int elem_bytes, int num_sms,
+                               cudaStream_t st);
+// out[t] = sum_{j<k} src[row(t*k+j)] in fp32, j ascending; k <= 32.  A slot
+// with an out-of-range expert id contributes nothing.
+cudaError_t launch_combine(const void* src, int H, int k, int E, const int* idx, const int* inv,
+                           const int* offsets, const int* poff, int64_t T, int64_t rows_max,
+                           void* out,
+                           int elem_bytes, int num_sms, cudaStream_t st);
+// d_topk_w[s] = sum_{n < ntiles} dwpart[n * rows_max + row(s)], n ascending.
+cudaError_t launch_dw_reduce(const float* dwpart, int ntiles, int64_t rows_max, int E,
+                             const int* idx,
+                             const int* inv, const int* offsets, const int* poff, int64_t Tk,
+                             float* d_topk_w, cudaStream_t st);
+
+// ---- grouped tensor-core GEMMs (gemm_*.cu)
+enum GemmMode : int {
+  kFwdGateUp = 0,    // A_act = act(Xp Wgu[e]) (+ saved pre-activations)
+  kFwdDown = 1,      // Ow = w * (A_act Wd[e])
+  kDgradDown = 2,    // dA' = dYp Wd[e]^T -> dH1, Aw, d(topk w) partials
+  kDgradGateUp = 3,  // dXp = dH1 Wgu[e]^T
+  kWgradDown = 4,    // dWd[e] = Aw^T dYp
+  kWgradGateUp = 5   // dWgu[e] = Xp^T dH1
+};
+
+struct GemmArgs {
+  const int* poff;      // [E+1] tile-padded row offsets
+  const int* counts;    // [E]
+  const int* offsets;   // [E+1]
+  const int* perm;      // [T*k]
+  const float* topk_w;  // [T*k]
+  int tk;               // T*k
+  int E;
+  int n_tiles;          // output-column tiles per expert
+  int m_tiles;          // weight-gradient modes: 128-row tiles of the output
+  int num_kb;           // row-grouped modes: 128-byte k-blocks of the contraction
+  int act;
+  float limit;
+  float alpha;
+  int save_h1;          // kFwdGateUp: also store the gate / up pre-activations
+  const void* h1;       // kDgradDown: saved pre-activations [rows_max, 2I]
+  int I;
+  float* dwpart;        // kDgradDown: [n_tiles][rows_max]
+  int64_t rows_max;
+  int* err;
+  uint64_t timeout_ns;
+};
+
+// maps: A, B0, B1, O0, O1, O2 (unused ones may repeat a valid map).
+cudaError_t launch_gemm(int mode, int elem_bytes, const CUtensorMap* maps, const GemmArgs& args,
+                        int num_sms, cudaStream_t st);
+// Column tile width (N) of the output for a mode, as used by launch_gemm.
+int gemm_block_n(int mode, int elem_bytes);
+
+}  // namespace moe

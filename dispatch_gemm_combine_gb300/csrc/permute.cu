@@ -1,0 +1,200 @@
+// Row movement between token order and the tile-padded expert-grouped order:
+//   gather   ("sparse token extraction" / "each token is repeated k times")
+//   combine  (the accumulate-back step the dispatch-and-combine page does with
+//             index_add_; here a k-way gather-sum per token in a fixed order,
+//             so no float atomics and bitwise-reproducible results)
+//   dw_reduce (fixed-order sum of the per-column-tile partial dot products
+//             that make d(topk weights))
+// All three are HBM-bound: one warp per row, 16-byte vector accesses,
+// grid sized as a multiple of the SM count.
+#include "kernels.h"
+
+namespace moe {
+
+// Expert whose padded segment holds row p: largest e with poff[e] <= p.
+__device__ __forceinline__ int expert_of_row(const int* __restrict__ poff, int E, int p) {
+  int lo = 0, hi = E - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (__ldg(poff + mid) <= p)
+      lo = mid;
+    else
+      hi = mid - 1;
+  }
+  return lo;
+}
+
+// Row of slot s in the padded layout, or -1 when the slot's expert id is out
+// of range or the row falls outside the expert's live rows (an inconsistent
+// plan): such slots contribute nothing instead of reading out of bounds.
+__device__ __forceinline__ int64_t padded_row_of_slot(int s, int E, const int* __restrict__ idx,
+                                                      const int* __restrict__ inv,
+                                                      const int* __restrict__ offsets,
+                                                      const int* __restrict__ poff) {
+  const int e = __ldg(idx + s);
+  if (e < 0 || e >= E) return -1;
+  const int local = __ldg(inv + s) - __ldg(offsets + e);
+  if (local < 0 || local >= __ldg(offsets + e + 1) - __ldg(offsets + e)) return -1;
+  return static_cast<int64_t>(__ldg(poff + e)) + local;
+}
+
+__global__ void __launch_bounds__(256) gather_rows_kernel(
+    const uint4* __restrict__ src, int vec_per_row, int k, int E, const int* __restrict__ poff,
+    const int* __restrict__ counts, const int* __restrict__ offsets, const int* __restrict__ perm,
+    int tk, int64_t rows_max, uint4* __restrict__ dst) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+  // never past the workspace bound, even for an inconsistent caller plan
+  const int64_t rows = min(static_cast<int64_t>(__ldg(poff + E)), rows_max);
+  for (int64_t p = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+       p < rows; p += warps) {
+    const int e = expert_of_row(poff, E, static_cast<int>(p));
+    const int local = static_cast<int>(p) - __ldg(poff + e);
+    uint4* d = dst + p * vec_per_row;
+    const int gi = __ldg(offsets + e) + local;
+    const int slot = (local < __ldg(counts + e) && gi < tk) ? __ldg(perm + gi) : -1;
+    if (slot >= 0 && slot < tk) {
+      const uint4* sr = src + static_cast<int64_t>(slot / k) * vec_per_row;
+      for (int v = lane; v < vec_per_row; v += 32) d[v] = __ldg(sr + v);
+    } else {
+      const uint4 z = make_uint4(0, 0, 0, 0);
+      for (int v = lane; v < vec_per_row; v += 32) d[v] = z;
+    }
+  }
+}
+
+template <typename T>
+struct Vec8;  // 16 bytes of T
+template <>
+struct Vec8<__nv_bfloat16> {
+  static constexpr int N = 8;
+  __device__ static void add(float* acc, uint4 v) {
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 f = __bfloat1622float2(h[i]);
+      acc[2 * i] += f.x;
+      acc[2 * i + 1] += f.y;
+    }
+  }
+  __device__ static uint4 pack(const float* acc) {
+    uint4 v;
+    __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&v);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) h[i] = __floats2bfloat162_rn(acc[2 * i], acc[2 * i + 1]);
+    return v;
+  }
+};
+template <>
+struct Vec8<float> {
+  static constexpr int N = 4;
+  __device__ static void add(float* acc, uint4 v) {
+    acc[0] += __uint_as_float(v.x);
+    acc[1] += __uint_as_float(v.y);
+    acc[2] += __uint_as_float(v.z);
+    acc[3] += __uint_as_float(v.w);
+  }
+  __device__ static uint4 pack(const float* acc) {
+    return make_uint4(__float_as_uint(acc[0]), __float_as_uint(acc[1]), __float_as_uint(acc[2]),
+                      __float_as_uint(acc[3]));
+  }
+};
+
+constexpr int kMaxK = 32;
+
+template <typename T>
+__global__ void __launch_bounds__(256) combine_kernel(const uint4* __restrict__ src,
+                                                      int vec_per_row, int k, int E,
+                                                      const int* __restrict__ idx,
+                                                      const int* __restrict__ inv,
+                                                      const int* __restrict__ offsets,
+                                                      const int* __restrict__ poff, int64_t T_,
+                                                      int64_t rows_max, uint4* __restrict__ out) {
+  __shared__ int64_t rows_s[8][kMaxK];   // padded rows of the current token's k slots
+  const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
+  const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+  for (int64_t t = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + wib; t < T_;
+       t += warps) {
+    if (lane < k)
+      rows_s[wib][lane] =
+          padded_row_of_slot(static_cast<int>(t * k + lane), E, idx, inv, offsets, poff);
+    __syncwarp();
+    for (int v = lane; v < vec_per_row; v += 32) {
+      float acc[Vec8<T>::N];
+#pragma unroll
+      for (int i = 0; i < Vec8<T>::N; ++i) acc[i] = 0.f;
+      for (int j = 0; j < k; ++j) {
+        const int64_t r = rows_s[wib][j];
+        if (r >= 0 && r < rows_max) Vec8<T>::add(acc, __ldg(src + r * vec_per_row + v));
+      }
+      out[t * vec_per_row + v] = Vec8<T>::pack(acc);
+    }
+    __syncwarp();
+  }
+}
+
+__global__ void __launch_bounds__(256) dw_reduce_kernel(const float* __restrict__ dwpart,
+                                                        int ntiles, int64_t rows_max, int E,
+                                                        const int* __restrict__ idx,
+                                                        const int* __restrict__ inv,
+                                                        const int* __restrict__ offsets,
+                                                        const int* __restrict__ poff, int64_t Tk,
+                                                        float* __restrict__ d_topk_w) {
+  const int64_t s = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (s >= Tk) return;
+  const int64_t p = padded_row_of_slot(static_cast<int>(s), E, idx, inv, offsets, poff);
+  float acc = 0.f;
+  if (p >= 0 && p < rows_max)
+    for (int n = 0; n < ntiles; ++n) acc += __ldg(dwpart + n * rows_max + p);
+  d_topk_w[s] = acc;
+}
+
+static int grid_for(int64_t rows, int num_sms) {
+  // 8 warps per block; enough blocks to cover every SM several times.
+  const int64_t need = (rows + 7) / 8;
+  int64_t g = static_cast<int64_t>(num_sms) * 8;
+  if (need < g) g = need > 0 ? need : 1;
+  return static_cast<int>(g);
+}
+
+cudaError_t launch_gather_rows(const void* src, int H, int k, int E, const int* poff,
+                               const int* counts, const int* offsets, const int* perm, int tk,
+                               int64_t rows_max, void* dst, int elem_bytes, int num_sms,
+                               cudaStream_t st) {
+  const int vec = H * elem_bytes / 16;
+  gather_rows_kernel<<<grid_for(rows_max, num_sms), 256, 0, st>>>(
+      static_cast<const uint4*>(src), vec, k, E, poff, counts, offsets, perm, tk, rows_max,
+      static_cast<uint4*>(dst));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_combine(const void* src, int H, int k, int E, const int* idx, const int* inv,
+                           const int* offsets, const int* poff, int64_t T, int64_t rows_max,
+                           void* out,
+                           int elem_bytes, int num_sms, cudaStream_t st) {
+  if (T == 0) return cudaSuccess;
+  if (k > kMaxK) return cudaErrorInvalidValue;
+  const int vec = H * elem_bytes / 16;
+  if (elem_bytes == 2)
+    combine_kernel<__nv_bfloat16><<<grid_for(T, num_sms), 256, 0, st>>>(
+        static_cast<const uint4*>(src), vec, k, E, idx, inv, offsets, poff, T, rows_max,
+        static_cast<uint4*>(out));
+  else
+    combine_kernel<float><<<grid_for(T, num_sms), 256, 0, st>>>(
+        static_cast<const uint4*>(src), vec, k, E, idx, inv, offsets, poff, T, rows_max,
+        static_cast<uint4*>(out));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dw_reduce(const float* dwpart, int ntiles, int64_t rows_max, int E,
+                             const int* idx,
+                             const int* inv, const int* offsets, const int* poff, int64_t Tk,
+                             float* d_topk_w, cudaStream_t st) {
+  if (Tk == 0) return cudaSuccess;
+  const int blocks = static_cast<int>((Tk + 255) / 256);
+  dw_reduce_kernel<<<blocks, 256, 0, st>>>(dwpart, ntiles, rows_max, E, idx, inv, offsets, poff,
+                                           Tk, d_topk_w);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

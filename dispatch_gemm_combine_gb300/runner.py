@@ -1,0 +1,54 @@
+"""Buffer management around the C ABI for one problem shape.
+
+`LayerRunner` allocates (through PyTorch) the plan arrays, workspaces, the
+saved context and the outputs for a fixed shape once, then runs
+moe_plan / moe_ffn_fwd / moe_ffn_bwd on them.  All arithmetic happens in the
+library's kernels.
+"""
+
+import torch
+
+from . import (MOE_BF16, MOE_FP32, Shape, alloc_plan, check_device_error, ffn_bwd, ffn_fwd,
+               moe_saved_size, plan, workspace)
+
+_TORCH_DTYPE = {MOE_BF16: torch.bfloat16, MOE_FP32: torch.float32}
+
+
+class LayerRunner:
+    def __init__(self, T, H, I, E, k, act, dtype=MOE_BF16, clamp_limit=7.0, alpha=1.702,
+                 device="cuda", training=True, backward=True):
+        self.shape = Shape(T, H, I, E, k, act, dtype, clamp_limit, alpha)
+        self.device = device
+        self.tdtype = _TORCH_DTYPE[dtype]
+        self.plan_t, self.plan_s = alloc_plan(self.shape, device)
+        self.ws_plan = workspace(self.shape, 0, device)
+        self.ws_fwd = workspace(self.shape, 1, device)
+        self.ws_bwd = workspace(self.shape, 2, device) if backward else None
+        self.saved = (torch.empty(moe_saved_size(self.shape), dtype=torch.uint8, device=device)
+                      if training else None)
+        self.y = torch.empty((T, H), dtype=self.tdtype, device=device)
+        if backward:
+            self.dx = torch.empty((T, H), dtype=self.tdtype, device=device)
+            self.d_topk_w = torch.empty((T, k), dtype=torch.float32, device=device)
+            self.dw_gate_up = torch.empty((E, H, 2 * I), dtype=torch.float32, device=device)
+            self.dw_down = torch.empty((E, I, H), dtype=torch.float32, device=device)
+
+    def plan(self, topk_idx, stream=None):
+        plan(self.shape, topk_idx, self.plan_s, self.ws_plan, stream)
+
+    def forward(self, x, topk_idx, topk_w, w_gate_up, w_down, use_plan=True, stream=None):
+        """y = layer(x).  With use_plan the plan must have been built by plan();
+        otherwise the forward builds its own inside the workspace."""
+        ffn_fwd(self.shape, x, topk_idx, topk_w, w_gate_up, w_down, self.y, self.ws_fwd,
+                self.plan_s if use_plan else None, self.saved, stream)
+        return self.y
+
+    def backward(self, dy, x, topk_idx, topk_w, w_gate_up, w_down, stream=None):
+        ffn_bwd(self.shape, dy, x, topk_idx, topk_w, w_gate_up, w_down, self.plan_s, self.saved,
+                self.dx, self.d_topk_w, self.dw_gate_up, self.dw_down, self.ws_bwd, stream)
+        return self.dx, self.d_topk_w, self.dw_gate_up, self.dw_down
+
+    def check(self, stream=None):
+        for ws in (self.ws_plan, self.ws_fwd, self.ws_bwd):
+            if ws is not None:
+                check_device_error(ws, stream)

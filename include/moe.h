@@ -1,0 +1,163 @@
+/*
+ * moe.h — C ABI of the GB300 (sm_103a) MoE expert layer.
+ *
+ * The layer (kernel-records pages "Sparse expert dispatch and combine",
+ * "MoE training token repeat and expert computation", "MoE expert parallel
+ * execution backward", each page's description):
+ *
+ *   given hidden states x[T,H], per token k expert ids idx[T,k] and routing
+ *   weights w[T,k], expert weights Wgu[E,H,2I] (gate = columns [0,I),
+ *   up = columns [I,2I)) and Wd[E,I,H],
+ *
+ *     y[t] = sum_j w[t,j] * ( act(x[t] Wgu[e] [:, :I], x[t] Wgu[e] [:, I:]) Wd[e] ),
+ *            e = idx[t,j],
+ *
+ *   with act = SwiGLU  (a = silu(g) * u)  or the clamped GLU
+ *   (a = (clamp(u,-L,L) + 1) * min(g,L) * sigmoid(alpha * min(g,L))).
+ *   The backward returns dx, d(topk weights), dWgu (d_gate = [:,:,:I],
+ *   d_up = [:,:,I:]) and dWd, the gradients of <dy, y>.
+ *
+ * General conventions
+ *   - Every pointer argument is a DEVICE pointer (cudaMalloc / torch), except
+ *     the `moe_shape` and `moe_plan_t` structs themselves, which live in host
+ *     memory.  Tensors are dense row-major; the caller owns all memory.  The
+ *     library never allocates device memory and keeps no state other than a
+ *     per-device cache of kernel attributes.
+ *   - Calls are asynchronous on `stream` (0 = legacy default stream).  The
+ *     return value reports host-side validation and launch failures.  Errors
+ *     found on the device (an expert id outside [0,E), a pipeline wait that
+ *     timed out) are recorded in a word inside the workspace and read with
+ *     moe_get_device_error(); outputs of such a call are undefined.
+ *   - Outputs are overwritten, never accumulated into.
+ *   - dtype MOE_BF16: x, y, dy, dx, Wgu, Wd are bfloat16; matrix products run
+ *     on the tensor cores with fp32 accumulation.  dtype MOE_FP32: those
+ *     tensors are float32 and the products run as TF32 with fp32
+ *     accumulation.  topk weights, d(topk weights) and the weight gradients
+ *     are always float32; expert ids are int32.
+ *   - Requirements: T >= 0, 1 <= k <= E <= 1024, T*k < 2^31, H and I
+ *     multiples of 8 (16-byte rows for the tensor-memory-access unit),
+ *     16-byte aligned pointers.  T = 0 is allowed: outputs with a T extent
+ *     are empty, the weight gradients are zero-filled.
+ *   - Workspace: `ws` of at least moe_workspace_size(shape, which) bytes,
+ *     256-byte aligned, zero-filled by the caller before its FIRST use (the
+ *     device error word lives in it).  One workspace must not be used by two
+ *     calls that may run concurrently.
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* moe_stream_t;   /* same type as cudaStream_t */
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,   /* a null pointer, a bad dimension, misalignment */
+  MOE_ERR_UNSUPPORTED = 2,   /* no sm_103a device, or a case not built */
+  MOE_ERR_WORKSPACE = 3,     /* ws_bytes below moe_workspace_size() */
+  MOE_ERR_BAD_INDEX = 4,     /* device: an expert id outside [0, E) */
+  MOE_ERR_TIMEOUT = 5,       /* device: a pipeline wait ran out of time */
+  MOE_ERR_CUDA = 6           /* a CUDA runtime / driver call failed */
+} moe_status;
+
+typedef enum { MOE_ACT_SWIGLU = 0, MOE_ACT_CLAMPED_GLU = 1 } moe_act;
+typedef enum { MOE_BF16 = 0, MOE_FP32 = 1 } moe_dtype;
+
+/* Problem description (model dimensions named on the pages' workload lines:
+ * hidden_size H, intermediate size I, number of experts E,
+ * num_experts_per_tok k).  clamp_limit / alpha are used by the clamped GLU
+ * only (7.0 / 1.702 in the workloads). */
+typedef struct {
+  int64_t T;
+  int32_t H, I, E, k;
+  int32_t act;          /* moe_act */
+  float clamp_limit;
+  float alpha;
+  int32_t dtype;        /* moe_dtype */
+} moe_shape;
+
+/* Dispatch plan ("masked indexing" / "sparse token extraction" in the pages'
+ * descriptions).  Slot s = t*k + j is token t's j-th choice.  Rows of the
+ * expert-grouped order are sorted by expert id, and by slot within an
+ * expert, so the plan is unique:
+ *   counts[e]   number of slots routed to expert e            [E]
+ *   offsets[e]  exclusive prefix sum of counts                [E+1]
+ *   perm[r]     slot held by grouped row r                    [T*k]
+ *   inv[s]      grouped row of slot s (inv[perm[r]] = r)      [T*k]
+ * All four are int32 device arrays owned by the caller. */
+typedef struct {
+  int32_t* counts;
+  int32_t* offsets;
+  int32_t* perm;
+  int32_t* inv;
+} moe_plan_t;
+
+/* Bytes of workspace needed by one call: which = 0 moe_plan, 1 moe_ffn_fwd,
+ * 2 moe_ffn_bwd.  Returns 0 for an invalid shape or `which`. */
+size_t moe_workspace_size(const moe_shape* shape, int which);
+
+/* Bytes of the context the training forward saves for the backward (the
+ * gate_up pre-activations, in the library's expert-grouped, tile-padded row
+ * order).  Returns 0 for an invalid shape. */
+size_t moe_saved_size(const moe_shape* shape);
+
+/* Build the dispatch plan of topk_idx [T,k] (int32, device).
+ * Writes plan->counts/offsets/perm/inv.  An id outside [0,E) records
+ * MOE_ERR_BAD_INDEX in the workspace; the plan is then undefined. */
+moe_status moe_plan(const moe_shape* shape, const int32_t* topk_idx,
+                    const moe_plan_t* plan, void* ws, size_t ws_bytes,
+                    moe_stream_t stream);
+
+/* Forward pass (dispatch -> gate_up GEMM + activation -> down GEMM with the
+ * routing-weight scale -> deterministic k-way combine).
+ *   x [T,H], topk_idx [T,k] int32, topk_w [T,k] fp32, w_gate_up [E,H,2I],
+ *   w_down [E,I,H]  -> y [T,H].
+ *   plan: a plan built by moe_plan for this topk_idx, or NULL to build one
+ *         inside the workspace.
+ *   saved: NULL (inference) or a buffer of moe_saved_size() bytes that
+ *          receives the context moe_ffn_bwd needs (training).
+ * The combine sums each token's k expert outputs in fp32 in the order
+ * j = 0..k-1 (no atomics): results are bitwise reproducible. */
+moe_status moe_ffn_fwd(const moe_shape* shape, const void* x,
+                       const int32_t* topk_idx, const float* topk_w,
+                       const void* w_gate_up, const void* w_down,
+                       const moe_plan_t* plan, void* y, void* saved,
+                       void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* Backward pass of <dy, y>.
+ *   dy [T,H]; x, topk_idx, topk_w, w_gate_up, w_down as given to the
+ *   forward; plan: the plan of topk_idx (required); saved: the context the
+ *   training forward wrote (required).
+ *   Outputs: dx [T,H]; d_topk_w [T,k] fp32; dw_gate_up [E,H,2I] fp32
+ *   (d_gate = [:,:,:I], d_up = [:,:,I:]); dw_down [E,I,H] fp32.  Experts
+ *   with no routed token get zero weight gradients.  All reductions run in
+ *   a fixed order (no float atomics). */
+moe_status moe_ffn_bwd(const moe_shape* shape, const void* dy, const void* x,
+                       const int32_t* topk_idx, const float* topk_w,
+                       const void* w_gate_up, const void* w_down,
+                       const moe_plan_t* plan, const void* saved,
+                       void* dx, float* d_topk_w, float* dw_gate_up,
+                       float* dw_down, void* ws, size_t ws_bytes,
+                       moe_stream_t stream);
+
+/* Synchronise `stream`, return the first device-side error recorded in the
+ * workspace since the last call (MOE_OK if none) and clear it. */
+moe_status moe_get_device_error(void* ws, moe_stream_t stream);
+
+/* Upper bound, in nanoseconds, on any single pipeline wait inside the GEMM
+ * kernels before they give up and record MOE_ERR_TIMEOUT (default 2 s).
+ * Process-wide; returns the previous value. */
+uint64_t moe_set_wait_timeout_ns(uint64_t ns);
+
+/* Static description of a status code. */
+const char* moe_status_string(moe_status status);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_GB300_H */

@@ -1,0 +1,164 @@
+"""GPU parity: the CUDA path through the C ABI against the fp64 oracle on the
+same seeded inputs, element by element.  Sizes span several 128-row tiles
+per expert, several column tiles, k-block tails (H, I not multiples of 64 or
+256) and the degenerate cases of the layer."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from synth import ACT_CLAMPED_GLU, ACT_SWIGLU, Recipe
+from tests.helpers import assert_close, assert_dw_close, oracle_inputs, to_device
+
+pytestmark = pytest.mark.gpu
+
+
+def _runner(r, training=True, backward=True):
+    from dispatch_gemm_combine_gb300 import MOE_BF16, MOE_FP32
+    from dispatch_gemm_combine_gb300.runner import LayerRunner
+    return LayerRunner(r.T, r.H, r.I, r.E, r.k, r.act,
+                       MOE_FP32 if r.dtype == "fp32" else MOE_BF16, r.limit, r.alpha,
+                       training=training, backward=backward)
+
+
+def _recipe(T, H, I, E, k, act, seed, dtype="bf16", routing="softmax_topk_renorm", std=None):
+    return Recipe("t", T=T, H=H, I=I, E=E, k=k, act=act, dtype=dtype,
+                  weight_std=std if std is not None else "fan_in", routing=routing, seed=seed)
+
+
+# ------------------------------------------------------------------- plan
+PLAN_CASES = [
+    # T, k, E, routing
+    (1, 1, 1, "uniform_ids"),
+    (7, 2, 5, "uniform_ids"),
+    (300, 4, 8, "softmax_topk_renorm"),
+    (1000, 8, 256, "softmax_topk_renorm"),      # several 1024-slot chunks
+    (2500, 3, 16, "uniform_ids"),                # duplicates within a token allowed
+    (3000, 8, 256, "zipf"),                      # skewed, ~30% experts empty
+    (4096, 8, 1024, "uniform_ids"),
+]
+
+
+@pytest.mark.parametrize("T,k,E,routing", PLAN_CASES)
+def test_plan_bit_exact(T, k, E, routing):
+    r = _recipe(T, 64, 64, E, k, ACT_SWIGLU, seed=T + E, routing=routing)
+    case = synth.make_case(r, with_dy=False)
+    run = _runner(r, training=False, backward=False)
+    idx = case.topk_idx.cuda()
+    run.plan(idx)
+    run.check()
+    counts, offsets, perm, inv = oracle.dispatch_plan(case.topk_idx.numpy(), E)
+    assert np.array_equal(run.plan_t["counts"].cpu().numpy(), counts)
+    assert np.array_equal(run.plan_t["offsets"].cpu().numpy(), offsets)
+    assert np.array_equal(run.plan_t["perm"].cpu().numpy()[:T * k], perm)
+    assert np.array_equal(run.plan_t["inv"].cpu().numpy()[:T * k], inv)
+
+
+def test_plan_all_tokens_one_expert():
+    T, k, E = 2000, 1, 16
+    idx = torch.full((T, k), 11, dtype=torch.int32)
+    r = _recipe(T, 64, 64, E, k, ACT_SWIGLU, seed=0)
+    run = _runner(r, training=False, backward=False)
+    run.plan(idx.cuda())
+    run.check()
+    counts, offsets, perm, inv = oracle.dispatch_plan(idx.numpy(), E)
+    assert np.array_equal(run.plan_t["counts"].cpu().numpy(), counts)
+    assert np.array_equal(run.plan_t["perm"].cpu().numpy(), perm)
+    assert np.array_equal(run.plan_t["inv"].cpu().numpy(), inv)
+
+
+# ------------------------------------------------------------------- forward / backward
+FB_CASES = [
+    # T, H, I, E, k, act, dtype, std, routing
+    (512, 384, 320, 8, 4, ACT_SWIGLU, "bf16", None, "softmax_topk_renorm"),
+    (512, 384, 320, 8, 4, ACT_CLAMPED_GLU, "bf16", 0.2, "uniform_topk_softmax"),
+    (300, 136, 200, 6, 2, ACT_SWIGLU, "bf16", None, "uniform_ids"),   # K tails, N tails
+    (64, 128, 128, 8, 2, ACT_SWIGLU, "fp32", None, "softmax_topk_renorm"),  # tiny fp32 recipe
+    (200, 264, 136, 5, 3, ACT_CLAMPED_GLU, "fp32", 0.2, "uniform_ids"),
+    (1, 64, 64, 4, 1, ACT_SWIGLU, "bf16", None, "uniform_ids"),       # a single token
+    (700, 256, 256, 40, 8, ACT_SWIGLU, "bf16", None, "zipf"),         # empty experts, hot expert
+]
+
+
+def _run_case(r, with_bwd=True, use_plan=True):
+    case = synth.make_case(r, with_dy=with_bwd)
+    d = to_device(case)
+    run = _runner(r, training=with_bwd, backward=with_bwd)
+    if use_plan:
+        run.plan(d.topk_idx)
+    y = run.forward(d.x, d.topk_idx, d.topk_w, d.w_gate_up, d.w_down, use_plan=use_plan)
+    grads = None
+    if with_bwd:
+        if not use_plan:
+            run.plan(d.topk_idx)
+        grads = run.backward(d.dy, d.x, d.topk_idx, d.topk_w, d.w_gate_up, d.w_down)
+    torch.cuda.synchronize()
+    run.check()
+    return case, y, grads
+
+
+@pytest.mark.parametrize("T,H,I,E,k,act,dtype,std,routing", FB_CASES)
+def test_forward_backward_parity(T, H, I, E, k, act, dtype, std, routing):
+    r = _recipe(T, H, I, E, k, act, seed=1000 + T, dtype=dtype, routing=routing, std=std)
+    case, y, grads = _run_case(r)
+    x, idx, w, wgu, wd, dy = oracle_inputs(case)
+    y_ref = oracle.moe_forward(x, idx, w, wgu, wd, act)
+    assert_close("y", y.float().cpu().numpy(), y_ref)
+    dx_ref, dw_ref, dwgu_ref, dwd_ref = oracle.moe_backward(dy, x, idx, w, wgu, wd, act)
+    dx, dtw, dwgu, dwd = grads
+    assert_close("dx", dx.float().cpu().numpy(), dx_ref)
+    assert_dw_close(dtw.cpu().numpy(), dw_ref)
+    assert_close("d_gate", dwgu[:, :, :I].cpu().numpy(), dwgu_ref[:, :, :I])
+    assert_close("d_up", dwgu[:, :, I:].cpu().numpy(), dwgu_ref[:, :, I:])
+    assert_close("d_down", dwd.cpu().numpy(), dwd_ref)
+    # experts that received no token get exactly zero weight gradients
+    counts = np.bincount(idx.reshape(-1), minlength=E)
+    for e in np.nonzero(counts == 0)[0]:
+        assert torch.all(dwgu[e] == 0) and torch.all(dwd[e] == 0)
+
+
+def test_forward_internal_plan_matches_external():
+    r = _recipe(333, 128, 192, 6, 3, ACT_CLAMPED_GLU, seed=5, std=0.2, routing="uniform_ids")
+    _, y1, _ = _run_case(r, with_bwd=False, use_plan=True)
+    _, y2, _ = _run_case(r, with_bwd=False, use_plan=False)
+    assert torch.equal(y1, y2)
+
+
+def test_forward_is_deterministic():
+    r = _recipe(1024, 256, 256, 16, 4, ACT_SWIGLU, seed=9)
+    case = synth.make_case(r)
+    d = to_device(case)
+    run = _runner(r)
+    run.plan(d.topk_idx)
+    outs = []
+    for _ in range(3):
+        y = run.forward(d.x, d.topk_idx, d.topk_w, d.w_gate_up, d.w_down).clone()
+        g = [t.clone() for t in run.backward(d.dy, d.x, d.topk_idx, d.topk_w, d.w_gate_up,
+                                             d.w_down)]
+        outs.append((y, g))
+    run.check()
+    for y, g in outs[1:]:
+        assert torch.equal(y, outs[0][0])
+        for a, b in zip(g, outs[0][1]):
+            assert torch.equal(a, b)
+
+
+def test_zero_tokens():
+    from dispatch_gemm_combine_gb300 import MOE_BF16, Shape, alloc_plan, ffn_bwd, ffn_fwd, workspace
+    from dispatch_gemm_combine_gb300.runner import LayerRunner
+    run = LayerRunner(0, 64, 64, 4, 2, ACT_SWIGLU, MOE_BF16)
+    x = torch.empty((0, 64), dtype=torch.bfloat16, device="cuda")
+    idx = torch.empty((0, 2), dtype=torch.int32, device="cuda")
+    w = torch.empty((0, 2), dtype=torch.float32, device="cuda")
+    wgu = torch.randn((4, 64, 128), device="cuda").bfloat16()
+    wd = torch.randn((4, 64, 64), device="cuda").bfloat16()
+    run.dw_gate_up.fill_(1.0)
+    run.dw_down.fill_(1.0)
+    run.plan(idx)
+    run.forward(x, idx, w, wgu, wd)
+    run.backward(x, x, idx, w, wgu, wd)
+    torch.cuda.synchronize()
+    run.check()
+    assert torch.all(run.dw_gate_up == 0) and torch.all(run.dw_down == 0)
