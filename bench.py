@@ -1,0 +1,501 @@
+#!/usr/bin/env python3
+"""Benchmark of the MoE expert layer on GB300.
+
+One step = one pass of the whole layer: dispatch plan, training forward
+(gather, gate_up GEMM + clamped GLU, down GEMM + routing weight, combine) and
+backward (both dgrads with the activation backward, d(topk weights), both
+fp32 weight gradients, dX combine), on the dispatch-and-combine workload
+(T=8192 tokens, H=I=2880, 128 experts, top-4, clamped GLU, bf16).  Inputs are
+seeded synthetic data resident in HBM; the 6.4 GB of expert weights exceed
+the 129 MB L2, so no flush is needed between steps.
+
+Prints ONE JSON line (rank 0).  `--impl reference` times the fp64 CPU oracle
+instead (the reference arm: there is no reference implementation to run).
+
+Run: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+For N > 1 launch one process per GPU with torch.distributed.run; every rank
+runs an independent replica (weak scaling, no data-path collective).
+"""
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+WORKLOAD = "clamped_glu_fwd"
+
+# ---------------------------------------------------------------- accounting
+
+
+def layer_flops(r):
+    """Forward 2*Tk*3*H*I, backward twice that (useful work only)."""
+    fwd = 2.0 * r.T * r.k * 3 * r.H * r.I
+    return fwd, 2.0 * fwd
+
+
+def layer_bytes(r, e_active):
+    """Algorithmic bytes of the layer: what the method must move.
+    forward : x + y + active-expert weights + routing ids/weights
+    backward: dy + x + dx + active weights + saved pre-activations (bf16
+              equivalent) + fp32 weight gradients of every expert + routing"""
+    es = 2 if r.dtype == "bf16" else 4
+    Tk = r.T * r.k
+    w_act = e_active * 3.0 * r.H * r.I * es
+    routing = Tk * 8.0
+    fwd = 2.0 * r.T * r.H * es + w_act + routing
+    bwd = 3.0 * r.T * r.H * es + w_act + Tk * 2.0 * r.I * es + r.E * 3.0 * r.H * r.I * 4 + routing
+    return fwd, bwd
+
+
+def kernel_work(r, e_active):
+    """Per-launch algorithmic FLOPs and compulsory bytes of each kernel kind
+    (its operands and outputs at their stored precision, useful rows only)."""
+    es = 2 if r.dtype == "bf16" else 4
+    T, H, I, E, k = r.T, r.H, r.I, r.E, r.k
+    Tk = T * k
+    wgu = e_active * H * 2.0 * I * es
+    wd = e_active * I * H * es
+    return {
+        "gather_rows": (0.0, T * H * es + Tk * H * es),
+        "gemm_fwd_gate_up_act": (4.0 * Tk * H * I, Tk * H * es + wgu + Tk * I * es + Tk * 2 * I * 4),
+        "gemm_fwd_down_scale": (2.0 * Tk * I * H, Tk * I * es + wd + Tk * H * 4),
+        "combine": (0.0, Tk * H * 4.0 + T * H * es),
+        "gemm_dgrad_down_act_bwd": (2.0 * Tk * H * I,
+                                    Tk * H * es + wd + Tk * 2 * I * 4 + Tk * 3 * I * es * 2),
+        "gemm_wgrad_down": (2.0 * Tk * I * H, Tk * I * es * 2 + Tk * H * es + E * I * H * 4.0),
+        "gemm_dgrad_gate_up": (4.0 * Tk * I * H, Tk * 2 * I * es + wgu + Tk * H * 4),
+        "gemm_wgrad_gate_up": (4.0 * Tk * H * I, Tk * H * es + Tk * 2 * I * es * 2 + E * H * 2.0 * I * 4),
+    }
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        try:
+            d = json.load(open(p))
+            out = {}
+            for key in ("hbm_gbs", "bf16_tflops", "bf16_tflops_sustained"):
+                v = d.get(key)
+                if isinstance(v, dict):
+                    v = v.get("value")
+                if v is not None:
+                    out[key] = float(v)
+            if "hbm_gbs" in out and "bf16_tflops" in out:
+                out.setdefault("bf16_tflops_sustained", out["bf16_tflops"])
+                return out, "measured"
+        except Exception:
+            pass
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def csrc_hash():
+    h = hashlib.sha256()
+    d = os.path.join(ROOT, "dispatch_gemm_combine_gb300", "csrc")
+    for f in sorted(os.listdir(d)):
+        if f.endswith((".cu", ".cuh", ".h")):
+            h.update(open(os.path.join(d, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def committed_traffic(kernel):
+    """Per-launch DRAM bytes of `kernel` on this workload from a committed ncu
+    summary, if it was taken on the current kernel sources; else None."""
+    p = os.path.join(ROOT, "profiles", "%s_%s.txt" % (kernel, WORKLOAD))
+    if not os.path.exists(p):
+        return None
+    kv = {}
+    for line in open(p):
+        if "=" in line and not line.startswith("#"):
+            a, b = line.split("=", 1)
+            kv[a.strip()] = b.strip()
+    if kv.get("source_hash") != csrc_hash():
+        return None
+    try:
+        return float(kv["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+# ---------------------------------------------------------------- clocks
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples every 200 ms while running."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.lines = []
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+
+    def summary(self):
+        return summarize_clocks(self.lines)
+
+
+def summarize_clocks(lines):
+    sm, smax, reasons = [], [], set()
+    names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    for ln in lines:
+        parts = [p.strip() for p in ln.split(",")]
+        if len(parts) < 9:
+            continue
+        try:
+            sm.append(float(parts[1]))
+            smax.append(float(parts[2]))
+        except ValueError:
+            continue
+        for n, v in zip(names, parts[5:9]):
+            if v.lower().startswith("active"):
+                reasons.add(n)
+    if not sm:
+        return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+    return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+            "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- CPU oracle leg
+
+
+class _LazyExperts:
+    """Expert weights fetched from the device one expert at a time (fp32)."""
+
+    def __init__(self, t):
+        self.t = t
+
+    def __len__(self):
+        return self.t.shape[0]
+
+    def __getitem__(self, e):
+        return self.t[e].float().cpu().numpy()
+
+
+def oracle_step(case, n_tok):
+    """One fp64 oracle pass (forward + backward) over the first n_tok tokens."""
+    import numpy as np
+    import oracle
+    r = case.recipe
+    x = case.x[:n_tok].float().cpu().numpy()
+    idx = case.topk_idx[:n_tok].cpu().numpy().astype(np.int64)
+    w = case.topk_w[:n_tok].cpu().numpy()
+    dy = case.dy[:n_tok].float().cpu().numpy()
+    wgu, wd = _LazyExperts(case.w_gate_up), _LazyExperts(case.w_down)
+    t0 = time.perf_counter()
+    oracle.moe_forward(x, idx, w, wgu, wd, r.act, r.limit, r.alpha)
+    oracle.moe_backward(dy, x, idx, w, wgu, wd, r.act, r.limit, r.alpha)
+    return time.perf_counter() - t0
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count()
+
+
+def pick_sample(case, target_s):
+    """Token count whose oracle pass takes about target_s seconds."""
+    n = 64
+    t = oracle_step(case, n)
+    n2 = int(n * target_s / max(t, 1e-3))
+    return max(16, min(case.recipe.T, n2))
+
+
+# ---------------------------------------------------------------- main
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=WORKLOAD)
+    ap.add_argument("--cpu-seconds", type=float, default=15.0,
+                    help="target length of the oracle sample (cpu_baseline)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    import torch
+    import synth
+
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        return run_reference(args, torch, synth)
+
+    import torch.distributed as dist
+    from dispatch_gemm_combine_gb300 import moe_kernel_launch_count, moe_profile_enable, moe_profile_read
+    from dispatch_gemm_combine_gb300.runner import LayerRunner
+    from dispatch_gemm_combine_gb300 import MOE_BF16, MOE_FP32
+
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl")
+    r = synth.RECIPES[args.workload]
+    case = synth.make_case(r, device="cuda")
+    dt = MOE_BF16 if r.dtype == "bf16" else MOE_FP32
+    run = LayerRunner(r.T, r.H, r.I, r.E, r.k, r.act, dt, r.limit, r.alpha)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        run.plan(case.topk_idx)
+        run.forward(case.x, case.topk_idx, case.topk_w, case.w_gate_up, case.w_down)
+        run.backward(case.dy, case.x, case.topk_idx, case.topk_w, case.w_gate_up, case.w_down)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    run.check()
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    def max_over_ranks(v):
+        if world == 1:
+            return v
+        t = torch.tensor([v], dtype=torch.float64, device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.6)
+    # ---- timed region: K steps, device time with CUDA events on the stream
+    barrier()
+    torch.cuda.synchronize()
+    n0 = moe_kernel_launch_count()
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    launches = moe_kernel_launch_count() - n0
+    clocks.stop()
+    ms = max_over_ranks(ev0.elapsed_time(ev1)) / args.steps
+    run.check()
+
+    # ---- per-kernel times (separate pass, library event timer on the same stream)
+    moe_profile_enable(True)
+    moe_profile_read()
+    nprof = max(3, min(args.steps, 20))
+    for _ in range(nprof):
+        step()
+    torch.cuda.synchronize()
+    prof = moe_profile_read()
+    moe_profile_enable(False)
+
+    # ---- fwd / bwd split
+    def timed(fn, n):
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(n):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / n
+
+    n_split = max(3, min(args.steps, 20))
+    fwd_ms = timed(lambda: (run.plan(case.topk_idx),
+                            run.forward(case.x, case.topk_idx, case.topk_w, case.w_gate_up,
+                                        case.w_down)), n_split)
+    bwd_ms = timed(lambda: run.backward(case.dy, case.x, case.topk_idx, case.topk_w,
+                                        case.w_gate_up, case.w_down), n_split)
+
+    # ---- end to end: pinned host inputs in, per-token results out, every step
+    h_in = {n: getattr(case, n).cpu().pin_memory() for n in ("x", "topk_idx", "topk_w", "dy")}
+    d_in = {n: torch.empty_like(getattr(case, n)) for n in h_in}
+    h_out = {"y": torch.empty(run.y.shape, dtype=run.y.dtype).pin_memory(),
+             "dx": torch.empty(run.dx.shape, dtype=run.dx.dtype).pin_memory(),
+             "d_topk_w": torch.empty(run.d_topk_w.shape, dtype=torch.float32).pin_memory()}
+    h2d = sum(t.numel() * t.element_size() for t in h_in.values())
+    d2h = sum(t.numel() * t.element_size() for t in h_out.values())
+
+    def e2e_step():
+        for n in h_in:
+            d_in[n].copy_(h_in[n], non_blocking=True)
+        run.plan(d_in["topk_idx"])
+        run.forward(d_in["x"], d_in["topk_idx"], d_in["topk_w"], case.w_gate_up, case.w_down)
+        run.backward(d_in["dy"], d_in["x"], d_in["topk_idx"], d_in["topk_w"], case.w_gate_up,
+                     case.w_down)
+        h_out["y"].copy_(run.y, non_blocking=True)
+        h_out["dx"].copy_(run.dx, non_blocking=True)
+        h_out["d_topk_w"].copy_(run.d_topk_w, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    n_e2e = max(3, min(args.steps, 50))
+    barrier()
+    e2e_ms = max_over_ranks(timed(e2e_step, n_e2e))
+    run.check()
+
+    # ---- accounting
+    e_active = int((run.plan_t["counts"] > 0).sum().item())
+    f_fwd, f_bwd = layer_flops(r)
+    b_fwd, b_bwd = layer_bytes(r, e_active)
+    peaks, peak_src = load_peaks()
+    P = peaks["bf16_tflops_sustained"] * 1e12
+    BW = peaks["hbm_gbs"] * 1e9
+    step_flops = f_fwd + f_bwd
+    value = world * step_flops / (ms * 1e-3) / 1e12
+
+    # dominant kernel and its roofline
+    work = kernel_work(r, e_active)
+    per_kernel = {}
+    for name, (tot, cnt) in prof.items():
+        if cnt:
+            per_kernel[name] = {"ms_per_launch": tot / cnt, "launches": cnt,
+                                "share": None}
+    tot_ms = sum(v["ms_per_launch"] * v["launches"] for v in per_kernel.values())
+    for v in per_kernel.values():
+        v["share"] = v["ms_per_launch"] * v["launches"] / tot_ms if tot_ms else None
+    dom = max(per_kernel, key=lambda n: per_kernel[n]["ms_per_launch"] * per_kernel[n]["launches"])
+    dflops, dbytes = work.get(dom, (0.0, 0.0))
+    dsec = per_kernel[dom]["ms_per_launch"] * 1e-3
+    tensor_bound = dflops / P > dbytes / BW
+    if tensor_bound:
+        achieved, peak, unit = dflops / dsec / 1e12, P / 1e12, "TFLOP/s"
+    else:
+        achieved, peak, unit = dbytes / dsec / 1e9, BW / 1e9, "GB/s"
+    roofline = {"kernel": dom, "bound": "tensor" if tensor_bound else "hbm",
+                "achieved": round(achieved, 1), "peak": peak, "unit": unit,
+                "frac": round(achieved / peak, 4), "traffic": committed_traffic(dom),
+                "algorithmic": dflops if tensor_bound else dbytes,
+                "peak_source": peak_src + (" sustained bf16" if tensor_bound else " hbm")}
+    for name, v in per_kernel.items():
+        fl, by = work.get(name, (0.0, 0.0))
+        s = v["ms_per_launch"] * 1e-3
+        v["tflops"] = round(fl / s / 1e12, 1) if fl else None
+        v["gbs"] = round(by / s / 1e9, 1) if by else None
+        v["ms_per_launch"] = round(v["ms_per_launch"], 4)
+        v["share"] = round(v["share"], 4) if v["share"] is not None else None
+
+    def layer_part(ms_, flops, byts):
+        roof = max(flops / P, byts / BW) * 1e3
+        return {"ms": round(ms_, 4), "tflops": round(flops / (ms_ * 1e-3) / 1e12, 1),
+                "roofline_ms": round(roof, 4), "frac": round(roof / ms_, 4),
+                "bound": "tensor" if flops / P > byts / BW else "hbm",
+                "algorithmic_bytes": byts, "flops": flops}
+
+    out = {
+        "metric": "MoE layer ms & TFLOP/s, % of bf16 tensor roofline (fwd and bwd)",
+        "value": round(value, 2),
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": r.dtype,
+        "data": "synthetic",
+        "config": {"workload": "%s fwd+bwd: T=%d H=%d I=%d E=%d top-%d clamped GLU (7.0, 1.702)"
+                   % (args.workload, r.T, r.H, r.I, r.E, r.k),
+                   "T": r.T, "H": r.H, "I": r.I, "E": r.E, "k": r.k, "seed": r.seed,
+                   "parallelism": "replicas" if world > 1 else "single GPU",
+                   "l2": "no flush: 6.4 GB of expert weights per step exceed the 129 MB L2"},
+        "layer": {"fwd": layer_part(fwd_ms, f_fwd, b_fwd), "bwd": layer_part(bwd_ms, f_bwd, b_bwd)},
+        "roofline": roofline,
+        "kernels": per_kernel,
+        "e2e": {"value": round(world * step_flops / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+                "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": int(launches),
+        "clocks": clocks.summary(),
+        "experts_active": e_active,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        n_tok = pick_sample(case, args.cpu_seconds)
+        t = oracle_step(case, n_tok)
+        fs = layer_flops(r.scaled(T=n_tok))
+        out["cpu_baseline"] = {"value": round((fs[0] + fs[1]) / t / 1e12, 5), "unit": "TFLOP/s",
+                               "cores": cpu_cores(), "kind": "oracle",
+                               "sample": "fp64 numpy oracle, fwd+bwd on the first %d of %d tokens "
+                                         "(all experts' weights), %.1f s" % (n_tok, r.T, t)}
+    if rank == 0:
+        print(json.dumps(out))
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def run_reference(args, torch, synth):
+    """Reference arm: the fp64 oracle on the host cores, each step a bounded
+    token sample of the same workload (inputs drawn on the GPU when present,
+    copied to the host one expert at a time)."""
+    r = synth.RECIPES[args.workload]
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    case = synth.make_case(r, device=dev)
+    per_step = max(1.0, 120.0 / max(1, args.steps + args.warmup))
+    n_tok = pick_sample(case, min(per_step, args.cpu_seconds))
+    for _ in range(args.warmup):
+        oracle_step(case, n_tok)
+    t = sum(oracle_step(case, n_tok) for _ in range(args.steps))
+    fs = layer_flops(r.scaled(T=n_tok))
+    value = args.steps * (fs[0] + fs[1]) / t / 1e12
+    sample = "fp64 numpy oracle, fwd+bwd on the first %d of %d tokens per step" % (n_tok, r.T)
+    out = {
+        "metric": "MoE layer ms & TFLOP/s, % of bf16 tensor roofline (fwd and bwd)",
+        "value": round(value, 5), "unit": "TFLOP/s", "n_gpus": args.gpus, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(1e3 * t / args.steps, 2),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "impl": "reference",
+        "config": {"workload": "%s fwd+bwd: T=%d H=%d I=%d E=%d top-%d clamped GLU (7.0, 1.702)"
+                   % (args.workload, r.T, r.H, r.I, r.E, r.k), "sample_tokens": n_tok},
+        "cpu_baseline": {"value": round(value, 5), "unit": "TFLOP/s", "cores": cpu_cores(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 5), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(out))
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

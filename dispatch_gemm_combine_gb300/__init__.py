@@ -18,7 +18,8 @@ __all__ = [
     "MOE_OK", "MOE_ACT_SWIGLU", "MOE_ACT_CLAMPED_GLU", "MOE_BF16", "MOE_FP32", "MoeShape",
     "MoePlan", "MoeError", "lib", "library_path", "moe_workspace_size", "moe_saved_size",
     "moe_plan", "moe_ffn_fwd", "moe_ffn_bwd", "moe_get_device_error", "moe_status_string",
-    "moe_set_wait_timeout_ns", "Shape", "alloc_plan", "workspace", "plan", "ffn_fwd", "ffn_bwd",
+    "moe_set_wait_timeout_ns", "moe_kernel_launch_count", "moe_profile_enable",
+    "moe_profile_read", "moe_profile_kernel_name", "Shape", "alloc_plan", "workspace", "plan", "ffn_fwd", "ffn_bwd",
     "check_device_error",
 ]
 
@@ -87,6 +88,15 @@ def lib():
     L.moe_status_string.restype = ctypes.c_char_p
     L.moe_set_wait_timeout_ns.argtypes = [ctypes.c_uint64]
     L.moe_set_wait_timeout_ns.restype = ctypes.c_uint64
+    L.moe_kernel_launch_count.argtypes = []
+    L.moe_kernel_launch_count.restype = ctypes.c_uint64
+    L.moe_profile_enable.argtypes = [ctypes.c_int]
+    L.moe_profile_enable.restype = ctypes.c_int
+    L.moe_profile_read.argtypes = [ctypes.POINTER(ctypes.c_double),
+                                   ctypes.POINTER(ctypes.c_uint64), ctypes.c_int]
+    L.moe_profile_read.restype = ctypes.c_int
+    L.moe_profile_kernel_name.argtypes = [ctypes.c_int]
+    L.moe_profile_kernel_name.restype = ctypes.c_char_p
     _lib = L
     return L
 
@@ -128,6 +138,28 @@ def moe_status_string(status):
 
 def moe_set_wait_timeout_ns(ns):
     return lib().moe_set_wait_timeout_ns(ns)
+
+
+def moe_kernel_launch_count():
+    return lib().moe_kernel_launch_count()
+
+
+def moe_profile_enable(on):
+    return lib().moe_profile_enable(1 if on else 0)
+
+
+def moe_profile_kernel_name(kind):
+    n = lib().moe_profile_kernel_name(kind)
+    return None if n is None else n.decode()
+
+
+def moe_profile_read():
+    """{kernel kind name: (total ms, launches)} since the last read."""
+    n = 32
+    ms = (ctypes.c_double * n)()
+    cnt = (ctypes.c_uint64 * n)()
+    k = lib().moe_profile_read(ms, cnt, n)
+    return {moe_profile_kernel_name(i): (ms[i], cnt[i]) for i in range(min(k, n))}
 
 
 # ---------------------------------------------------------------- torch helpers

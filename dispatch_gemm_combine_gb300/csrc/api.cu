@@ -16,18 +16,19 @@
 #include <atomic>
 #include <cstring>
 #include <mutex>
+#include <vector>
 
 #include "kernels.h"
 #include "moe.h"
 
 namespace moe {
 
-cudaError_t launch_gemm_bf16_fwd(int, const CUtensorMap*, const GemmArgs&, int, cudaStream_t);
-cudaError_t launch_gemm_bf16_dgrad(int, const CUtensorMap*, const GemmArgs&, int, cudaStream_t);
-cudaError_t launch_gemm_bf16_wgrad(int, const CUtensorMap*, const GemmArgs&, int, cudaStream_t);
-cudaError_t launch_gemm_f32(int, const CUtensorMap*, const GemmArgs&, int, cudaStream_t);
+cudaError_t launch_gemm_bf16_fwd(int, const GemmMaps&, const GemmArgs&, int, cudaStream_t);
+cudaError_t launch_gemm_bf16_dgrad(int, const GemmMaps&, const GemmArgs&, int, cudaStream_t);
+cudaError_t launch_gemm_bf16_wgrad(int, const GemmMaps&, const GemmArgs&, int, cudaStream_t);
+cudaError_t launch_gemm_f32(int, const GemmMaps&, const GemmArgs&, int, cudaStream_t);
 
-cudaError_t launch_gemm(int mode, int elem_bytes, const CUtensorMap* maps, const GemmArgs& args,
+cudaError_t launch_gemm(int mode, int elem_bytes, const GemmMaps& maps, const GemmArgs& args,
                         int num_sms, cudaStream_t st) {
   if (elem_bytes == 4) return launch_gemm_f32(mode, maps, args, num_sms, st);
   switch (mode) {
@@ -39,7 +40,12 @@ cudaError_t launch_gemm(int mode, int elem_bytes, const CUtensorMap* maps, const
   }
 }
 
-int gemm_block_n(int mode, int /*elem_bytes*/) { return mode == kFwdGateUp ? 128 : 256; }
+// Output-column tile width of each mode (must match the instantiations).
+int gemm_block_n(int mode, int elem_bytes) {
+  if (mode == kFwdGateUp) return 128;
+  if (mode == kWgradGateUp && elem_bytes == 2) return 128;
+  return 256;
+}
 
 }  // namespace moe
 
@@ -50,6 +56,61 @@ namespace {
 constexpr int kMaxExperts = 1024;
 constexpr int kMaxTopK = 32;
 std::atomic<uint64_t> g_timeout_ns{2000000000ull};
+
+// ------------------------------------------------------------ launch accounting
+// Kernel kinds, for the launch counter and the optional event timer.
+enum Kind : int {
+  kKPlan = 0, kKOffsets, kKGather, kKFwdGateUp, kKFwdDown, kKCombine, kKDgradDown, kKDwReduce,
+  kKWgradDown, kKDgradGateUp, kKWgradGateUp, kKMemset, kKTranspose, kNumKinds
+};
+const char* const kKindNames[kNumKinds] = {
+    "plan", "padded_offsets", "gather_rows", "gemm_fwd_gate_up_act", "gemm_fwd_down_scale",
+    "combine", "gemm_dgrad_down_act_bwd", "dw_reduce", "gemm_wgrad_down", "gemm_dgrad_gate_up",
+    "gemm_wgrad_gate_up", "memset", "transpose_f32"};
+
+std::atomic<uint64_t> g_launches{0};
+std::atomic<int> g_profile{0};
+struct ProfRec {
+  int kind;
+  cudaEvent_t a, b;
+};
+std::mutex g_prof_mu;
+std::vector<ProfRec> g_prof_pending;
+std::vector<cudaEvent_t> g_event_pool;
+double g_prof_ms[kNumKinds];
+uint64_t g_prof_n[kNumKinds];
+
+cudaEvent_t pool_event() {
+  if (!g_event_pool.empty()) {
+    cudaEvent_t e = g_event_pool.back();
+    g_event_pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+  return e;
+}
+
+// Run one launcher, counting its kernels and, when the timer is on,
+// bracketing it with events on the launching stream.
+template <typename F>
+cudaError_t tracked(int kind, int nkernels, cudaStream_t st, F&& launch) {
+  cudaEvent_t a = nullptr, b = nullptr;
+  if (g_profile.load(std::memory_order_relaxed)) {
+    std::lock_guard<std::mutex> lk(g_prof_mu);
+    a = pool_event();
+    b = pool_event();
+    if (a && b) cudaEventRecord(a, st);
+  }
+  const cudaError_t e = launch();
+  g_launches.fetch_add(static_cast<uint64_t>(nkernels), std::memory_order_relaxed);
+  if (a && b) {
+    cudaEventRecord(b, st);
+    std::lock_guard<std::mutex> lk(g_prof_mu);
+    g_prof_pending.push_back({kind, a, b});
+  }
+  return e;
+}
 
 // ------------------------------------------------------------ device cache
 struct DevInfo {
@@ -159,7 +220,10 @@ size_t align256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
 
 struct Layout {
   size_t err = 0, counts = 0, offsets = 0, perm = 0, inv = 0, poff = 0, blkhist = 0;
-  size_t xp = 0, act = 0, dyp = 0, dh1 = 0, aw = 0, dwpart = 0;
+  size_t xp = 0, act = 0, ow = 0, dyp = 0, dh1 = 0, dh1lo = 0, aw = 0, awlo = 0, dxp = 0;
+  size_t dwpart = 0;
+  // fp32 storage only: K-major copies for the TF32 products
+  size_t wguT = 0, wdT = 0, awT = 0, dypT = 0, xpT = 0, dh1T = 0, wdR = 0, wguR = 0;
   size_t total = 0;
 };
 
@@ -186,12 +250,29 @@ Layout layout(const moe_shape* s, int which) {
     L.inv = take(sizeof(int) * (Tk > 0 ? Tk : 1));
     L.xp = take(es * R * s->H);
     L.act = take(es * R * s->I);
+    L.ow = take(sizeof(float) * R * s->H);
+    if (es == 4) {
+      L.wguT = take(sizeof(float) * s->E * 2ull * s->I * s->H);
+      L.wdT = take(sizeof(float) * s->E * static_cast<size_t>(s->I) * s->H);
+    }
   }
   if (which == 2) {
     L.dyp = take(es * R * s->H);
     L.xp = take(es * R * s->H);
     L.dh1 = take(es * R * 2 * s->I);
     L.aw = take(es * R * s->I);
+    if (es == 2) {  // bf16 remainders of dH1 and w*a (operands of the weight gradients)
+      L.dh1lo = take(es * R * 2 * s->I);
+      L.awlo = take(es * R * s->I);
+    } else {
+      L.awT = take(es * R * s->I);
+      L.dypT = take(es * R * s->H);
+      L.xpT = take(es * R * s->H);
+      L.dh1T = take(es * R * 2 * s->I);
+      L.wdR = take(sizeof(float) * s->E * static_cast<size_t>(s->I) * s->H);
+      L.wguR = take(sizeof(float) * s->E * 2ull * s->I * s->H);
+    }
+    L.dxp = take(sizeof(float) * R * s->H);
     L.dwpart = take(sizeof(float) * R * dgrad_down_ntiles(s));
   }
   L.total = off;
@@ -244,10 +325,41 @@ size_t moe_workspace_size(const moe_shape* shape, int which) {
 size_t moe_saved_size(const moe_shape* shape) {
   if (!shape_ok(shape)) return 0;
   const size_t r = static_cast<size_t>(rows_max(shape));
-  return (r > 0 ? r : 1) * 2 * shape->I * elem_bytes(shape);
+  return (r > 0 ? r : 1) * 2 * shape->I * sizeof(float);   // fp32 gate | up pre-activations
 }
 
 uint64_t moe_set_wait_timeout_ns(uint64_t ns) { return g_timeout_ns.exchange(ns); }
+
+uint64_t moe_kernel_launch_count(void) { return g_launches.load(); }
+
+int moe_profile_enable(int on) { return g_profile.exchange(on ? 1 : 0); }
+
+const char* moe_profile_kernel_name(int kind) {
+  return (kind >= 0 && kind < kNumKinds) ? kKindNames[kind] : nullptr;
+}
+
+int moe_profile_read(double* total_ms, uint64_t* launches, int n) {
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  for (const ProfRec& r : g_prof_pending) {
+    float ms = 0.f;
+    if (cudaEventSynchronize(r.b) == cudaSuccess && cudaEventElapsedTime(&ms, r.a, r.b) == cudaSuccess) {
+      g_prof_ms[r.kind] += ms;
+      g_prof_n[r.kind] += 1;
+    }
+    g_event_pool.push_back(r.a);
+    g_event_pool.push_back(r.b);
+  }
+  g_prof_pending.clear();
+  for (int i = 0; i < kNumKinds && i < n; ++i) {
+    if (total_ms) total_ms[i] = g_prof_ms[i];
+    if (launches) launches[i] = g_prof_n[i];
+  }
+  for (int i = 0; i < kNumKinds; ++i) {
+    g_prof_ms[i] = 0.0;
+    g_prof_n[i] = 0;
+  }
+  return kNumKinds;
+}
 
 const char* moe_status_string(moe_status st) {
   switch (st) {
@@ -283,8 +395,10 @@ moe_status moe_plan(const moe_shape* s, const int32_t* topk_idx, const moe_plan_
   const moe_status ds = device_info(&sms);
   if (ds != MOE_OK) return ds;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  MOE_CUDA(launch_plan(topk_idx, Tk, s->E, plan->counts, plan->offsets, plan->perm, plan->inv,
-                       at<int>(ws, L.poff), at<int>(ws, L.blkhist), at<int>(ws, L.err), st));
+  MOE_CUDA(tracked(kKPlan, Tk > 0 ? 3 : 1, st, [&] {
+    return launch_plan(topk_idx, Tk, s->E, plan->counts, plan->offsets, plan->perm, plan->inv,
+                       at<int>(ws, L.poff), at<int>(ws, L.blkhist), at<int>(ws, L.err), st);
+  }));
   return MOE_OK;
 }
 
@@ -319,13 +433,15 @@ moe_status moe_ffn_fwd(const moe_shape* s, const void* x, const int32_t* topk_id
     offsets = plan->offsets;
     perm = plan->perm;
     inv = plan->inv;
-    MOE_CUDA(launch_padded_offsets(counts, E, poff, st));
+    MOE_CUDA(tracked(kKOffsets, 1, st, [&] { return launch_padded_offsets(counts, E, poff, st); }));
   } else {
     int* c = at<int>(ws, L.counts);
     int* o = at<int>(ws, L.offsets);
     int* p = at<int>(ws, L.perm);
     int* v = at<int>(ws, L.inv);
-    MOE_CUDA(launch_plan(topk_idx, Tk, E, c, o, p, v, poff, at<int>(ws, L.blkhist), err, st));
+    MOE_CUDA(tracked(kKPlan, 3, st, [&] {
+      return launch_plan(topk_idx, Tk, E, c, o, p, v, poff, at<int>(ws, L.blkhist), err, st);
+    }));
     counts = c;
     offsets = o;
     perm = p;
@@ -333,53 +449,77 @@ moe_status moe_ffn_fwd(const moe_shape* s, const void* x, const int32_t* topk_id
   }
   void* xp = at<char>(ws, L.xp);
   void* aact = at<char>(ws, L.act);
-  MOE_CUDA(launch_gather_rows(x, H, s->k, E, poff, counts, offsets, perm, static_cast<int>(Tk), R, xp,
-                              es, sms, st));
+  MOE_CUDA(tracked(kKGather, 1, st, [&] {
+    return launch_gather_rows(x, H, s->k, E, poff, counts, offsets, perm, static_cast<int>(Tk),
+                              R, xp, es, sms, st);
+  }));
 
   const uint32_t BK = 128 / es, CH = 128 / es;
   const auto SW = CU_TENSOR_MAP_SWIZZLE_128B;
   const auto OSW = out_swizzle(es);
+  const auto OSW32 = out_swizzle(4);
   const char* wgu = static_cast<const char*>(w_gate_up);
 
-  // gate_up GEMM + activation
-  CUtensorMap m1[6];
-  bool ok = map2d(&m1[0], es, xp, H, R, H, BK, 128, SW) &&
-            map3d(&m1[1], es, wgu, I, H, E, 2ll * I, 2ll * I * H, CH, BK, SW) &&
-            map3d(&m1[2], es, wgu + static_cast<size_t>(I) * es, I, H, E, 2ll * I, 2ll * I * H,
-                  CH, BK, SW) &&
-            map2d(&m1[3], es, aact, I, R, I, 32, 32, OSW);
-  if (ok && saved) {
-    ok = map2d(&m1[4], es, saved, I, R, 2ll * I, 32, 32, OSW) &&
-         map2d(&m1[5], es, static_cast<char*>(saved) + static_cast<size_t>(I) * es, I, R, 2ll * I,
-               32, 32, OSW);
+  // gate_up GEMM + activation (+ fp32 pre-activations saved for the backward)
+  GemmMaps m1;
+  bool ok = map2d(&m1.a, es, xp, H, R, H, BK, 128, SW) && map2d(&m1.o[0], es, aact, I, R, I, 32, 32, OSW);
+  if (es == 2) {
+    ok = ok && map3d(&m1.b0, es, wgu, I, H, E, 2ll * I, 2ll * I * H, CH, BK, SW) &&
+         map3d(&m1.b1, es, wgu + static_cast<size_t>(I) * es, I, H, E, 2ll * I, 2ll * I * H, CH,
+               BK, SW);
   } else {
-    m1[4] = m1[3];
-    m1[5] = m1[3];
+    // TF32 takes K-major operands only: use the transposed weights [E, 2I, H]
+    float* wguT = at<float>(ws, L.wguT);
+    MOE_CUDA(tracked(kKTranspose, 1, st, [&] {
+      return launch_transpose_f32(static_cast<const float*>(w_gate_up), wguT, E, H, 2 * I, st);
+    }));
+    ok = ok && map3d(&m1.b0, es, wguT, H, I, E, H, 2ll * I * H, BK, 128, SW) &&
+         map3d(&m1.b1, es, wguT + static_cast<size_t>(I) * H, H, I, E, H, 2ll * I * H, BK, 128,
+               SW);
+  }
+  if (ok && saved) {
+    ok = map2d(&m1.o[1], 4, saved, I, R, 2ll * I, 32, 32, OSW32) &&
+         map2d(&m1.o[2], 4, static_cast<char*>(saved) + static_cast<size_t>(I) * 4, I, R, 2ll * I,
+               32, 32, OSW32);
+  } else {
+    m1.o[1] = m1.o[0];
+    m1.o[2] = m1.o[0];
   }
   if (!ok) return MOE_ERR_CUDA;
+  m1.a2 = m1.a;
+  for (int i = 3; i < 6; ++i) m1.o[i] = m1.o[0];
   GemmArgs a1 = base_args(s, poff, counts, offsets, perm, topk_w, err);
   a1.num_kb = (H + BK - 1) / BK;
   a1.n_tiles = (I + gemm_block_n(kFwdGateUp, es) - 1) / gemm_block_n(kFwdGateUp, es);
   a1.save_h1 = saved ? 1 : 0;
-  MOE_CUDA(launch_gemm(kFwdGateUp, es, m1, a1, sms, st));
+  MOE_CUDA(tracked(kKFwdGateUp, 1, st, [&] { return launch_gemm(kFwdGateUp, es, m1, a1, sms, st); }));
 
-  // down GEMM * routing weight -> Ow (reuses the Xp buffer)
-  void* ow = xp;
-  CUtensorMap m2[6];
-  ok = map2d(&m2[0], es, aact, I, R, I, BK, 128, SW) &&
-       map3d(&m2[1], es, w_down, H, I, E, H, static_cast<int64_t>(H) * I, CH, BK, SW) &&
-       map2d(&m2[3], es, ow, H, R, H, 32, 32, OSW);
+  // down GEMM * routing weight -> fp32 rows Ow
+  float* ow = at<float>(ws, L.ow);
+  GemmMaps m2;
+  ok = map2d(&m2.a, es, aact, I, R, I, BK, 128, SW) && map2d(&m2.o[0], 4, ow, H, R, H, 32, 32, OSW32);
+  if (es == 2) {
+    ok = ok && map3d(&m2.b0, es, w_down, H, I, E, H, static_cast<int64_t>(H) * I, CH, BK, SW);
+  } else {
+    float* wdT = at<float>(ws, L.wdT);
+    MOE_CUDA(tracked(kKTranspose, 1, st, [&] {
+      return launch_transpose_f32(static_cast<const float*>(w_down), wdT, E, I, H, st);
+    }));
+    ok = ok && map3d(&m2.b0, es, wdT, I, H, E, I, static_cast<int64_t>(H) * I, BK, 256, SW);
+  }
   if (!ok) return MOE_ERR_CUDA;
-  m2[2] = m2[1];
-  m2[4] = m2[3];
-  m2[5] = m2[3];
+  m2.a2 = m2.a;
+  m2.b1 = m2.b0;
+  for (int i = 1; i < 6; ++i) m2.o[i] = m2.o[0];
   GemmArgs a2 = base_args(s, poff, counts, offsets, perm, topk_w, err);
   a2.num_kb = (I + BK - 1) / BK;
   a2.n_tiles = (H + gemm_block_n(kFwdDown, es) - 1) / gemm_block_n(kFwdDown, es);
-  MOE_CUDA(launch_gemm(kFwdDown, es, m2, a2, sms, st));
+  MOE_CUDA(tracked(kKFwdDown, 1, st, [&] { return launch_gemm(kFwdDown, es, m2, a2, sms, st); }));
 
   // combine
-  MOE_CUDA(launch_combine(ow, H, s->k, E, topk_idx, inv, offsets, poff, s->T, R, y, es, sms, st));
+  MOE_CUDA(tracked(kKCombine, 1, st, [&] {
+    return launch_combine(ow, H, s->k, E, topk_idx, inv, offsets, poff, s->T, R, y, es, sms, st);
+  }));
   return MOE_OK;
 }
 
@@ -397,8 +537,11 @@ moe_status moe_ffn_bwd(const moe_shape* s, const void* dy, const void* x, const 
   const int es = elem_bytes(s);
   const int H = s->H, I = s->I, E = s->E;
   if (s->T == 0) {
-    MOE_CUDA(cudaMemsetAsync(dw_gate_up, 0, sizeof(float) * E * H * 2ull * I, st));
-    MOE_CUDA(cudaMemsetAsync(dw_down, 0, sizeof(float) * E * static_cast<size_t>(I) * H, st));
+    MOE_CUDA(tracked(kKMemset, 2, st, [&] {
+      cudaError_t e1 = cudaMemsetAsync(dw_gate_up, 0, sizeof(float) * E * H * 2ull * I, st);
+      cudaError_t e2 = cudaMemsetAsync(dw_down, 0, sizeof(float) * E * static_cast<size_t>(I) * H, st);
+      return e1 != cudaSuccess ? e1 : e2;
+    }));
     return MOE_OK;
   }
   if (!dy || !x || !topk_idx || !topk_w || !plan || !saved || !dx || !d_topk_w)
@@ -419,84 +562,146 @@ moe_status moe_ffn_bwd(const moe_shape* s, const void* dy, const void* x, const 
   const int* offsets = plan->offsets;
   const int* perm = plan->perm;
   const int* inv = plan->inv;
-  MOE_CUDA(launch_padded_offsets(counts, E, poff, st));
+  MOE_CUDA(tracked(kKOffsets, 1, st, [&] { return launch_padded_offsets(counts, E, poff, st); }));
 
   void* dyp = at<char>(ws, L.dyp);
   void* xp = at<char>(ws, L.xp);
   void* dh1 = at<char>(ws, L.dh1);
   void* aw = at<char>(ws, L.aw);
+  const bool split = (es == 2);
+  void* dh1lo = split ? at<char>(ws, L.dh1lo) : dh1;
+  void* awlo = split ? at<char>(ws, L.awlo) : aw;
   float* dwpart = at<float>(ws, L.dwpart);
-  MOE_CUDA(launch_gather_rows(dy, H, s->k, E, poff, counts, offsets, perm, static_cast<int>(Tk), R,
-                              dyp, es, sms, st));
-  MOE_CUDA(launch_gather_rows(x, H, s->k, E, poff, counts, offsets, perm, static_cast<int>(Tk), R, xp,
-                              es, sms, st));
+  MOE_CUDA(tracked(kKGather, 1, st, [&] {
+    return launch_gather_rows(dy, H, s->k, E, poff, counts, offsets, perm, static_cast<int>(Tk),
+                              R, dyp, es, sms, st);
+  }));
+  MOE_CUDA(tracked(kKGather, 1, st, [&] {
+    return launch_gather_rows(x, H, s->k, E, poff, counts, offsets, perm, static_cast<int>(Tk),
+                              R, xp, es, sms, st);
+  }));
 
   const uint32_t BK = 128 / es, CH = 128 / es;
   const auto SW = CU_TENSOR_MAP_SWIZZLE_128B;
   const auto OSW = out_swizzle(es);
   const auto OSW32 = out_swizzle(4);
-  const char* dh1c = static_cast<const char*>(dh1);
+  const size_t up_off = static_cast<size_t>(I) * es;
   bool ok;
 
-  // (1) down dgrad + activation backward -> dH1 (gate | up), Aw, dw partials
-  CUtensorMap m1[6];
-  ok = map2d(&m1[0], es, dyp, H, R, H, BK, 128, SW) &&
-       map3d(&m1[1], es, w_down, H, I, E, H, static_cast<int64_t>(H) * I, BK, 256, SW) &&
-       map2d(&m1[3], es, dh1, I, R, 2ll * I, 32, 32, OSW) &&
-       map2d(&m1[4], es, dh1c + static_cast<size_t>(I) * es, I, R, 2ll * I, 32, 32, OSW) &&
-       map2d(&m1[5], es, aw, I, R, I, 32, 32, OSW);
+  // TF32 reads only the top bits of fp32 operands: give the dgrads
+  // round-to-nearest copies of the weights.
+  const void* wd_op = w_down;
+  const void* wgu_op = w_gate_up;
+  if (!split) {
+    float* wdR = at<float>(ws, L.wdR);
+    float* wguR = at<float>(ws, L.wguR);
+    MOE_CUDA(tracked(kKTranspose, 2, st, [&] {
+      cudaError_t e1 = launch_round_copy_tf32(static_cast<const float*>(w_down), wdR,
+                                              static_cast<int64_t>(E) * I * H, sms, st);
+      cudaError_t e2 = launch_round_copy_tf32(static_cast<const float*>(w_gate_up), wguR,
+                                              static_cast<int64_t>(E) * 2 * I * H, sms, st);
+      return e1 != cudaSuccess ? e1 : e2;
+    }));
+    wd_op = wdR;
+    wgu_op = wguR;
+  }
+
+  // (1) down dgrad + activation backward -> dH1 (gate | up), w*a, dw partials
+  GemmMaps m1;
+  ok = map2d(&m1.a, es, dyp, H, R, H, BK, 128, SW) &&
+       map3d(&m1.b0, es, wd_op, H, I, E, H, static_cast<int64_t>(H) * I, BK, 256, SW) &&
+       map2d(&m1.o[0], es, dh1, I, R, 2ll * I, 32, 32, OSW) &&
+       map2d(&m1.o[1], es, static_cast<char*>(dh1) + up_off, I, R, 2ll * I, 32, 32, OSW) &&
+       map2d(&m1.o[2], es, aw, I, R, I, 32, 32, OSW) &&
+       map2d(&m1.o[3], es, dh1lo, I, R, 2ll * I, 32, 32, OSW) &&
+       map2d(&m1.o[4], es, static_cast<char*>(dh1lo) + up_off, I, R, 2ll * I, 32, 32, OSW) &&
+       map2d(&m1.o[5], es, awlo, I, R, I, 32, 32, OSW);
   if (!ok) return MOE_ERR_CUDA;
-  m1[2] = m1[1];
+  m1.a2 = m1.a;
+  m1.b1 = m1.b0;
   GemmArgs a1 = base_args(s, poff, counts, offsets, perm, topk_w, err);
   a1.num_kb = (H + BK - 1) / BK;
   a1.n_tiles = dgrad_down_ntiles(s);
   a1.h1 = saved;
   a1.dwpart = dwpart;
-  MOE_CUDA(launch_gemm(kDgradDown, es, m1, a1, sms, st));
-  MOE_CUDA(launch_dw_reduce(dwpart, a1.n_tiles, R, E, topk_idx, inv, offsets, poff, Tk, d_topk_w, st));
+  MOE_CUDA(tracked(kKDgradDown, 1, st, [&] { return launch_gemm(kDgradDown, es, m1, a1, sms, st); }));
+  MOE_CUDA(tracked(kKDwReduce, 1, st, [&] {
+    return launch_dw_reduce(dwpart, a1.n_tiles, R, E, topk_idx, inv, offsets, poff, Tk, d_topk_w,
+                            st);
+  }));
 
-  // (2) down wgrad: dWd[e] = Aw_e^T dYp_e
-  CUtensorMap m2[6];
-  ok = map2d(&m2[0], es, aw, I, R, I, CH, BK, SW) && map2d(&m2[1], es, dyp, H, R, H, CH, BK, SW) &&
-       map3d(&m2[3], 4, dw_down, H, I, E, H, static_cast<int64_t>(H) * I, 32, 32, OSW32);
+  // (2) down wgrad: dWd[e] = (w*a)_e^T dYp_e  (w*a as a bf16 hi/lo pair)
+  GemmMaps m2;
+  ok = map3d(&m2.o[0], 4, dw_down, H, I, E, H, static_cast<int64_t>(H) * I, 32, 32, OSW32);
+  if (split) {
+    ok = ok && map2d(&m2.a, es, aw, I, R, I, CH, BK, SW) &&
+         map2d(&m2.a2, es, awlo, I, R, I, CH, BK, SW) && map2d(&m2.b0, es, dyp, H, R, H, CH, BK, SW);
+  } else {
+    // TF32: K-major copies [I, R] and [H, R] of the row-major activations
+    float* awT = at<float>(ws, L.awT);
+    float* dypT = at<float>(ws, L.dypT);
+    MOE_CUDA(tracked(kKTranspose, 2, st, [&] {
+      cudaError_t e1 = launch_transpose_f32(static_cast<const float*>(aw), awT, 1, R, I, st);
+      cudaError_t e2 = launch_transpose_f32(static_cast<const float*>(dyp), dypT, 1, R, H, st);
+      return e1 != cudaSuccess ? e1 : e2;
+    }));
+    ok = ok && map2d(&m2.a, es, awT, R, I, R, BK, 128, SW) &&
+         map2d(&m2.b0, es, dypT, R, H, R, BK, 256, SW);
+    m2.a2 = m2.a;
+  }
   if (!ok) return MOE_ERR_CUDA;
-  m2[2] = m2[1];
-  m2[4] = m2[3];
-  m2[5] = m2[3];
+  m2.b1 = m2.b0;
+  for (int i = 1; i < 6; ++i) m2.o[i] = m2.o[0];
   GemmArgs a2 = base_args(s, poff, counts, offsets, perm, topk_w, err);
   a2.m_tiles = (I + 127) / 128;
-  a2.n_tiles = (H + 255) / 256;
-  MOE_CUDA(launch_gemm(kWgradDown, es, m2, a2, sms, st));
+  a2.n_tiles = (H + gemm_block_n(kWgradDown, es) - 1) / gemm_block_n(kWgradDown, es);
+  MOE_CUDA(tracked(kKWgradDown, 1, st, [&] { return launch_gemm(kWgradDown, es, m2, a2, sms, st); }));
 
-  // (3) gate_up dgrad: dXp = dH1 Wgu[e]^T  (written over dYp)
-  void* dxp = dyp;
-  CUtensorMap m3[6];
-  ok = map2d(&m3[0], es, dh1, 2ll * I, R, 2ll * I, BK, 128, SW) &&
-       map3d(&m3[1], es, w_gate_up, 2ll * I, H, E, 2ll * I, 2ll * I * H, BK, 256, SW) &&
-       map2d(&m3[3], es, dxp, H, R, H, 32, 32, OSW);
+  // (3) gate_up dgrad: dXp = dH1 Wgu[e]^T  (fp32 rows for the combine)
+  float* dxp = at<float>(ws, L.dxp);
+  GemmMaps m3;
+  ok = map2d(&m3.a, es, dh1, 2ll * I, R, 2ll * I, BK, 128, SW) &&
+       map3d(&m3.b0, es, wgu_op, 2ll * I, H, E, 2ll * I, 2ll * I * H, BK, 256, SW) &&
+       map2d(&m3.o[0], 4, dxp, H, R, H, 32, 32, OSW32);
   if (!ok) return MOE_ERR_CUDA;
-  m3[2] = m3[1];
-  m3[4] = m3[3];
-  m3[5] = m3[3];
+  m3.a2 = m3.a;
+  m3.b1 = m3.b0;
+  for (int i = 1; i < 6; ++i) m3.o[i] = m3.o[0];
   GemmArgs a3 = base_args(s, poff, counts, offsets, perm, topk_w, err);
   a3.num_kb = (2 * I + BK - 1) / BK;
-  a3.n_tiles = (H + 255) / 256;
-  MOE_CUDA(launch_gemm(kDgradGateUp, es, m3, a3, sms, st));
-  MOE_CUDA(launch_combine(dxp, H, s->k, E, topk_idx, inv, offsets, poff, s->T, R, dx, es, sms, st));
+  a3.n_tiles = (H + gemm_block_n(kDgradGateUp, es) - 1) / gemm_block_n(kDgradGateUp, es);
+  MOE_CUDA(tracked(kKDgradGateUp, 1, st, [&] { return launch_gemm(kDgradGateUp, es, m3, a3, sms, st); }));
+  MOE_CUDA(tracked(kKCombine, 1, st, [&] {
+    return launch_combine(dxp, H, s->k, E, topk_idx, inv, offsets, poff, s->T, R, dx, es, sms, st);
+  }));
 
-  // (4) gate_up wgrad: dWgu[e] = Xp_e^T dH1_e
-  CUtensorMap m4[6];
-  ok = map2d(&m4[0], es, xp, H, R, H, CH, BK, SW) &&
-       map2d(&m4[1], es, dh1, 2ll * I, R, 2ll * I, CH, BK, SW) &&
-       map3d(&m4[3], 4, dw_gate_up, 2ll * I, H, E, 2ll * I, 2ll * I * H, 32, 32, OSW32);
+  // (4) gate_up wgrad: dWgu[e] = Xp_e^T dH1_e  (dH1 as a bf16 hi/lo pair)
+  const int bn4 = gemm_block_n(kWgradGateUp, es);
+  GemmMaps m4;
+  ok = map3d(&m4.o[0], 4, dw_gate_up, 2ll * I, H, E, 2ll * I, 2ll * I * H, 32, 32, OSW32);
+  if (split) {
+    ok = ok && map2d(&m4.a, es, xp, H, R, H, CH, BK, SW) &&
+         map2d(&m4.b0, es, dh1, 2ll * I, R, 2ll * I, CH, BK, SW) &&
+         map2d(&m4.b1, es, dh1lo, 2ll * I, R, 2ll * I, CH, BK, SW);
+  } else {
+    float* xpT = at<float>(ws, L.xpT);
+    float* dh1T = at<float>(ws, L.dh1T);
+    MOE_CUDA(tracked(kKTranspose, 2, st, [&] {
+      cudaError_t e1 = launch_transpose_f32(static_cast<const float*>(xp), xpT, 1, R, H, st);
+      cudaError_t e2 = launch_transpose_f32(static_cast<const float*>(dh1), dh1T, 1, R, 2 * I, st);
+      return e1 != cudaSuccess ? e1 : e2;
+    }));
+    ok = ok && map2d(&m4.a, es, xpT, R, H, R, BK, 128, SW) &&
+         map2d(&m4.b0, es, dh1T, R, 2ll * I, R, BK, 256, SW);
+    m4.b1 = m4.b0;
+  }
   if (!ok) return MOE_ERR_CUDA;
-  m4[2] = m4[1];
-  m4[4] = m4[3];
-  m4[5] = m4[3];
+  m4.a2 = m4.a;
+  for (int i = 1; i < 6; ++i) m4.o[i] = m4.o[0];
   GemmArgs a4 = base_args(s, poff, counts, offsets, perm, topk_w, err);
   a4.m_tiles = (H + 127) / 128;
-  a4.n_tiles = (2 * I + 255) / 256;
-  MOE_CUDA(launch_gemm(kWgradGateUp, es, m4, a4, sms, st));
+  a4.n_tiles = (2 * I + bn4 - 1) / bn4;
+  MOE_CUDA(tracked(kKWgradGateUp, 1, st, [&] { return launch_gemm(kWgradGateUp, es, m4, a4, sms, st); }));
   return MOE_OK;
 }
 

@@ -245,6 +245,15 @@ __host__ __device__ constexpr uint32_t make_idesc(bool tf32, bool a_mn, bool b_m
 // ---------------------------------------------------------------- numerics
 __device__ __forceinline__ float sigmoidf_(float z) { return 1.0f / (1.0f + __expf(-z)); }
 
+// Round an fp32 value to the nearest TF32 value (10-bit mantissa).  The
+// TF32 tensor-core path reads only the top bits of each fp32 operand, so
+// operands are rounded before they reach it instead of being truncated.
+__device__ __forceinline__ float round_tf32(float x) {
+  uint32_t r;
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+  return __uint_as_float(r);
+}
+
 template <typename T>
 __device__ __forceinline__ T from_f32(float v);
 template <>

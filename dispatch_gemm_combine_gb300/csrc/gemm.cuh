@@ -43,15 +43,27 @@ struct GemmCfg {
   static constexpr int MMA_K = 32 / kES;         // K of one tcgen05.mma
   static constexpr int KSTEPS = BK / MMA_K;      // MMAs per k-block (4)
   static constexpr bool kWgrad = (MODE == kWgradDown || MODE == kWgradGateUp);
-  static constexpr bool A_MN = kWgrad;
-  static constexpr bool B_MN = (MODE == kFwdGateUp || MODE == kFwdDown || kWgrad);
-  static constexpr int A_BYTES = BM * 128;
-  static constexpr int B_BYTES = BN * 128;
+  // TF32 operands must be K-major (the fp32 path transposes the others into
+  // the workspace first); 16-bit operands may be MN-major.
+  static constexpr bool A_MN = kWgrad && !kTf32;
+  static constexpr bool B_MN = (MODE == kFwdGateUp || MODE == kFwdDown || kWgrad) && !kTf32;
+  // bf16 weight gradients contract a computed operand (w*a, dH1) that is
+  // carried as a bf16 hi/lo pair: two MMAs, one per part, into the same
+  // accumulator (about 16 bits of mantissa instead of 8).
+  static constexpr bool SPLIT_A = (MODE == kWgradDown) && !kTf32;
+  static constexpr bool SPLIT_B = (MODE == kWgradGateUp) && !kTf32;
+  static constexpr int A_PART = BM * 128;
+  static constexpr int B_PART = BN * 128;
+  static constexpr int A_BYTES = A_PART * (SPLIT_A ? 2 : 1);
+  static constexpr int B_BYTES = B_PART * (SPLIT_B ? 2 : 1);
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int CHUNK_BYTES = BK * 128;   // one MN-major box
-  // output element size of the epilogue tiles
-  static constexpr int OUT_ES = kWgrad ? 4 : kES;
-  static constexpr int OUT_TILE = 32 * 32 * OUT_ES;
+  // 32x32 output staging tile: fp32 outputs (weight gradients, the saved
+  // fp32 pre-activations, the fp32 rows the combine sums, or fp32 storage)
+  // take 4 KB, 16-bit ones 2 KB.
+  static constexpr bool kOut32 =
+      kWgrad || kTf32 || MODE == kFwdGateUp || MODE == kFwdDown || MODE == kDgradGateUp;
+  static constexpr int OUT_TILE = 32 * 32 * (kOut32 ? 4 : 2);
   static constexpr int EPI_BYTES = 4 * NBUF * OUT_TILE;
   static constexpr int BAR_BYTES = (2 * STAGES + 5) * 8 + 16;
   static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + EPI_BYTES + BAR_BYTES;
@@ -168,14 +180,38 @@ __device__ __forceinline__ void stage_row(uint8_t* buf, int lane, const float (&
   }
 }
 
+// Stage one 32x32 output tile (this thread's row) and store it with TMA;
+// `buf` cycles through NBUF staging buffers of this warp.
+template <typename O, int NBUF, int OUT_TILE>
+__device__ __forceinline__ void emit_tile(const CUtensorMap* map, const float (&v)[32], int c0,
+                                          int c1, int c2, bool three_d, uint8_t* my_epi,
+                                          uint32_t my_epi_s, int& buf, int lane) {
+  if (lane == 0) bulk_wait_read<NBUF - 1>();
+  __syncwarp();
+  stage_row<O>(my_epi + buf * OUT_TILE, lane, v);
+  fence_async_shared();
+  __syncwarp();
+  if (lane == 0) {
+    const uint32_t bs = my_epi_s + buf * OUT_TILE;
+    if (three_d)
+      tma_store_3d(map, bs, c0, c1, c2);
+    else
+      tma_store_2d(map, bs, c0, c1);
+    bulk_commit();
+  }
+  __syncwarp();
+  if (++buf == NBUF) buf = 0;
+}
+
+__device__ __forceinline__ void split_bf16(float x, float& hi, float& lo) {
+  hi = __bfloat162float(__float2bfloat16_rn(x));
+  lo = x - hi;
+}
+
 template <typename T, int MODE, int BN, int STAGES, int NBUF>
 __global__ void __launch_bounds__(192, 1)
-    moe_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
-                    const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmO0,
-                    const __grid_constant__ CUtensorMap tmO1, const __grid_constant__ CUtensorMap tmO2,
-                    const GemmArgs args) {
+    moe_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs args) {
   using C = GemmCfg<T, MODE, BN, STAGES, NBUF>;
-  using OutT = typename std::conditional<C::kWgrad, float, T>::type;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t sbase = (raw + 1023u) & ~1023u;
@@ -206,9 +242,8 @@ __global__ void __launch_bounds__(192, 1)
     }
     mbar_init(drain_bar, 1);
     fence_barrier_init();
-    prefetch_tmap(&tmA);
-    prefetch_tmap(&tmB0);
-    prefetch_tmap(&tmB1);
+    prefetch_tmap(&maps.a);
+    prefetch_tmap(&maps.b0);
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, C::TMEM_COLS);
@@ -223,7 +258,8 @@ __global__ void __launch_bounds__(192, 1)
   if constexpr (C::kWgrad)
     total = args.E * args.m_tiles * args.n_tiles;
   else
-    total = static_cast<int>(min(static_cast<int64_t>(__ldg(args.poff + args.E)), args.rows_max) >> 7) *
+    total = static_cast<int>(min(static_cast<int64_t>(__ldg(args.poff + args.E)), args.rows_max) >>
+                             7) *
             args.n_tiles;
 
   const uint64_t tmo = args.timeout_ns;
@@ -251,31 +287,49 @@ __global__ void __launch_bounds__(192, 1)
           const uint32_t sB = sA + C::A_BYTES;
           mbar_arrive_expect_tx(fb, C::STAGE_BYTES);
           const int kc = kb * C::BK;
-          if constexpr (MODE == kFwdGateUp) {
-            tma_load_2d(sA, &tmA, fb, kc, ti.row0);
+          if constexpr (MODE == kFwdGateUp && C::B_MN) {
+            tma_load_2d(sA, &maps.a, fb, kc, ti.row0);
             constexpr int HALF_CH = (BN / 2) / C::CH;
 #pragma unroll
             for (int c = 0; c < HALF_CH; ++c) {
-              tma_load_3d(sB + c * C::CHUNK_BYTES, &tmB0, fb, ti.n0 + c * C::CH, kc, ti.e);
-              tma_load_3d(sB + (HALF_CH + c) * C::CHUNK_BYTES, &tmB1, fb, ti.n0 + c * C::CH, kc,
-                          ti.e);
+              tma_load_3d(sB + c * C::CHUNK_BYTES, &maps.b0, fb, ti.n0 + c * C::CH, kc, ti.e);
+              tma_load_3d(sB + (HALF_CH + c) * C::CHUNK_BYTES, &maps.b1, fb, ti.n0 + c * C::CH,
+                          kc, ti.e);
             }
-          } else if constexpr (MODE == kFwdDown) {
-            tma_load_2d(sA, &tmA, fb, kc, ti.row0);
+          } else if constexpr (MODE == kFwdGateUp) {
+            // K-major (transposed) weights: gate rows then up rows of the tile
+            tma_load_2d(sA, &maps.a, fb, kc, ti.row0);
+            tma_load_3d(sB, &maps.b0, fb, kc, ti.n0, ti.e);
+            tma_load_3d(sB + (BN / 2) * 128, &maps.b1, fb, kc, ti.n0, ti.e);
+          } else if constexpr (MODE == kFwdDown && C::B_MN) {
+            tma_load_2d(sA, &maps.a, fb, kc, ti.row0);
 #pragma unroll
             for (int c = 0; c < BN / C::CH; ++c)
-              tma_load_3d(sB + c * C::CHUNK_BYTES, &tmB0, fb, ti.n0 + c * C::CH, kc, ti.e);
-          } else if constexpr (MODE == kDgradDown || MODE == kDgradGateUp) {
-            tma_load_2d(sA, &tmA, fb, kc, ti.row0);
-            tma_load_3d(sB, &tmB0, fb, kc, ti.n0, ti.e);
+              tma_load_3d(sB + c * C::CHUNK_BYTES, &maps.b0, fb, ti.n0 + c * C::CH, kc, ti.e);
+          } else if constexpr (MODE == kFwdDown || MODE == kDgradDown || MODE == kDgradGateUp) {
+            tma_load_2d(sA, &maps.a, fb, kc, ti.row0);
+            tma_load_3d(sB, &maps.b0, fb, kc, ti.n0, ti.e);
+          } else if constexpr (!C::A_MN) {
+            // weight gradient from K-major (transposed) activations
+            const int r = ti.row0 + kc;
+            tma_load_2d(sA, &maps.a, fb, r, ti.m0);
+            tma_load_2d(sB, &maps.b0, fb, r, ti.n0);
           } else {
             const int r = ti.row0 + kc;
 #pragma unroll
-            for (int c = 0; c < 128 / C::CH; ++c)
-              tma_load_2d(sA + c * C::CHUNK_BYTES, &tmA, fb, ti.m0 + c * C::CH, r);
+            for (int c = 0; c < 128 / C::CH; ++c) {
+              tma_load_2d(sA + c * C::CHUNK_BYTES, &maps.a, fb, ti.m0 + c * C::CH, r);
+              if constexpr (C::SPLIT_A)
+                tma_load_2d(sA + C::A_PART + c * C::CHUNK_BYTES, &maps.a2, fb, ti.m0 + c * C::CH,
+                            r);
+            }
 #pragma unroll
-            for (int c = 0; c < BN / C::CH; ++c)
-              tma_load_2d(sB + c * C::CHUNK_BYTES, &tmB0, fb, ti.n0 + c * C::CH, r);
+            for (int c = 0; c < BN / C::CH; ++c) {
+              tma_load_2d(sB + c * C::CHUNK_BYTES, &maps.b0, fb, ti.n0 + c * C::CH, r);
+              if constexpr (C::SPLIT_B)
+                tma_load_2d(sB + C::B_PART + c * C::CHUNK_BYTES, &maps.b1, fb, ti.n0 + c * C::CH,
+                            r);
+            }
           }
         }
         __syncwarp();
@@ -328,16 +382,27 @@ __global__ void __launch_bounds__(192, 1)
           const uint32_t sB = sA + C::A_BYTES;
 #pragma unroll
           for (int kk = 0; kk < C::KSTEPS; ++kk) {
-            uint64_t adesc, bdesc;
+            uint32_t aoff, boff;
             if constexpr (C::A_MN)
-              adesc = smem_desc_sw128(sA + kk * C::MMA_K * 128, C::CHUNK_BYTES, 1024);
+              aoff = kk * C::MMA_K * 128;
             else
-              adesc = smem_desc_sw128(sA + kk * 32, 16, 1024);
+              aoff = kk * 32;
             if constexpr (C::B_MN)
-              bdesc = smem_desc_sw128(sB + kk * C::MMA_K * 128, C::CHUNK_BYTES, 1024);
+              boff = kk * C::MMA_K * 128;
             else
-              bdesc = smem_desc_sw128(sB + kk * 32, 16, 1024);
-            tc_mma<C::kTf32>(d_tmem, adesc, bdesc, C::IDESC, (kb | kk) != 0 ? 1u : 0u);
+              boff = kk * 32;
+            const uint32_t albo = C::A_MN ? C::CHUNK_BYTES : 16;
+            const uint32_t blbo = C::B_MN ? C::CHUNK_BYTES : 16;
+            const uint64_t adesc = smem_desc_sw128(sA + aoff, albo, 1024);
+            const uint64_t bdesc = smem_desc_sw128(sB + boff, blbo, 1024);
+            const uint32_t accum = (kb | kk) != 0 ? 1u : 0u;
+            tc_mma<C::kTf32>(d_tmem, adesc, bdesc, C::IDESC, accum);
+            if constexpr (C::SPLIT_A)
+              tc_mma<C::kTf32>(d_tmem, smem_desc_sw128(sA + C::A_PART + aoff, albo, 1024), bdesc,
+                               C::IDESC, 1u);
+            if constexpr (C::SPLIT_B)
+              tc_mma<C::kTf32>(d_tmem, adesc, smem_desc_sw128(sB + C::B_PART + boff, blbo, 1024),
+                               C::IDESC, 1u);
           }
           tc_commit(empty_bar + 8 * stage);
         }
@@ -378,27 +443,6 @@ __global__ void __launch_bounds__(192, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
 
-    // stage `v` as this warp's 32x32 tile and store it with TMA at (c0, c1[, c2])
-    auto emit = [&](const CUtensorMap* map, const float (&v)[32], int c0, int c1, int c2,
-                    bool three_d) {
-      if (lane == 0) bulk_wait_read<NBUF - 1>();
-      __syncwarp();
-      uint8_t* b = my_epi + buf * C::OUT_TILE;
-      stage_row<OutT>(b, lane, v);
-      fence_async_shared();
-      __syncwarp();
-      if (lane == 0) {
-        const uint32_t bs = my_epi_s + buf * C::OUT_TILE;
-        if (three_d)
-          tma_store_3d(map, bs, c0, c1, c2);
-        else
-          tma_store_2d(map, bs, c0, c1);
-        bulk_commit();
-      }
-      __syncwarp();
-      if (++buf == NBUF) buf = 0;
-    };
-
     for (int t = blockIdx.x; t < total; t += gridDim.x) {
       const TileInfo ti = decode_tile<C::BN_OUT, C::kWgrad>(args, t, C::BK);
       int good = 1;
@@ -411,6 +455,7 @@ __global__ void __launch_bounds__(192, 1)
       tc_fence_after();
       const uint32_t tacc = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
       const int row = ti.row0 + q * 32 + lane;   // row-grouped modes: padded row of this thread
+      const int orow = ti.row0 + q * 32;         // first row of this warp's output tiles
       float v[32];
 
       if constexpr (C::kWgrad) {
@@ -422,7 +467,8 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
             for (int i = 0; i < 32; ++i) v[i] = 0.f;
           }
-          emit(&tmO0, v, ti.n0 + c * 32, ti.m0 + q * 32, ti.e, true);
+          emit_tile<float, NBUF, C::OUT_TILE>(&maps.o[0], v, ti.n0 + c * 32, ti.m0 + q * 32, ti.e,
+                                              true, my_epi, my_epi_s, buf, lane);
         }
       } else {
         // routing weight and liveness of this thread's row
@@ -443,12 +489,18 @@ __global__ void __launch_bounds__(192, 1)
             tmem_ld32(tacc + c * 32, v);
             tmem_ld32(tacc + BN / 2 + c * 32, u);
             if (args.save_h1) {
-              emit(&tmO1, v, ti.n0 + c * 32, ti.row0 + q * 32, 0, false);
-              emit(&tmO2, u, ti.n0 + c * 32, ti.row0 + q * 32, 0, false);
+              emit_tile<float, NBUF, C::OUT_TILE>(&maps.o[1], v, ti.n0 + c * 32, orow, 0, false,
+                                                  my_epi, my_epi_s, buf, lane);
+              emit_tile<float, NBUF, C::OUT_TILE>(&maps.o[2], u, ti.n0 + c * 32, orow, 0, false,
+                                                  my_epi, my_epi_s, buf, lane);
             }
 #pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] = act_fwd<T>(args.act, v[i], u[i], args.limit, args.alpha);
-            emit(&tmO0, v, ti.n0 + c * 32, ti.row0 + q * 32, 0, false);
+            for (int i = 0; i < 32; ++i) {
+              v[i] = act_fwd<T>(args.act, v[i], u[i], args.limit, args.alpha);
+              if constexpr (C::kTf32) v[i] = round_tf32(v[i]);   // operand of the down GEMM
+            }
+            emit_tile<T, NBUF, C::OUT_TILE>(&maps.o[0], v, ti.n0 + c * 32, orow, 0, false, my_epi,
+                                            my_epi_s, buf, lane);
           }
         } else if constexpr (MODE == kFwdDown) {
 #pragma unroll 1
@@ -456,16 +508,19 @@ __global__ void __launch_bounds__(192, 1)
             tmem_ld32(tacc + c * 32, v);
 #pragma unroll
             for (int i = 0; i < 32; ++i) v[i] *= wrow;
-            emit(&tmO0, v, ti.n0 + c * 32, ti.row0 + q * 32, 0, false);
+            emit_tile<float, NBUF, C::OUT_TILE>(&maps.o[0], v, ti.n0 + c * 32, orow, 0, false,
+                                                my_epi, my_epi_s, buf, lane);
           }
         } else if constexpr (MODE == kDgradGateUp) {
 #pragma unroll 1
           for (int c = 0; c < BN / 32; ++c) {
             tmem_ld32(tacc + c * 32, v);
-            emit(&tmO0, v, ti.n0 + c * 32, ti.row0 + q * 32, 0, false);
+            emit_tile<float, NBUF, C::OUT_TILE>(&maps.o[0], v, ti.n0 + c * 32, orow, 0, false,
+                                                my_epi, my_epi_s, buf, lane);
           }
         } else {  // kDgradDown
-          const T* h1row = static_cast<const T*>(args.h1) + static_cast<int64_t>(row) * 2 * args.I;
+          // saved fp32 pre-activations of this row: gate at [0, I), up at [I, 2I)
+          const float* h1row = static_cast<const float*>(args.h1) + static_cast<int64_t>(row) * 2 * args.I;
           float dot = 0.f;
 #pragma unroll 1
           for (int c = 0; c < BN / 32; ++c) {
@@ -473,27 +528,21 @@ __global__ void __launch_bounds__(192, 1)
             const int i0 = ti.n0 + c * 32;
             float g[32], u[32];
             if (i0 + 32 <= args.I) {
-              const uint4* gp = reinterpret_cast<const uint4*>(h1row + i0);
-              const uint4* up = reinterpret_cast<const uint4*>(h1row + args.I + i0);
-              constexpr int NV = 32 * sizeof(T) / 16;
+              const float4* gp = reinterpret_cast<const float4*>(h1row + i0);
+              const float4* up = reinterpret_cast<const float4*>(h1row + args.I + i0);
 #pragma unroll
-              for (int j = 0; j < NV; ++j) {
-                const uint4 gv = __ldg(gp + j);
-                const uint4 uv = __ldg(up + j);
-                const T* gt = reinterpret_cast<const T*>(&gv);
-                const T* ut = reinterpret_cast<const T*>(&uv);
-#pragma unroll
-                for (int i = 0; i < 16 / static_cast<int>(sizeof(T)); ++i) {
-                  g[j * (16 / sizeof(T)) + i] = to_f32(gt[i]);
-                  u[j * (16 / sizeof(T)) + i] = to_f32(ut[i]);
-                }
+              for (int j = 0; j < 8; ++j) {
+                const float4 gv = __ldg(gp + j);
+                const float4 uv = __ldg(up + j);
+                g[4 * j] = gv.x; g[4 * j + 1] = gv.y; g[4 * j + 2] = gv.z; g[4 * j + 3] = gv.w;
+                u[4 * j] = uv.x; u[4 * j + 1] = uv.y; u[4 * j + 2] = uv.z; u[4 * j + 3] = uv.w;
               }
             } else {
 #pragma unroll
               for (int i = 0; i < 32; ++i) {
                 const bool in = (i0 + i) < args.I;
-                g[i] = in ? to_f32(h1row[i0 + i]) : 0.f;
-                u[i] = in ? to_f32(h1row[args.I + i0 + i]) : 0.f;
+                g[i] = in ? __ldg(h1row + i0 + i) : 0.f;
+                u[i] = in ? __ldg(h1row + args.I + i0 + i) : 0.f;
               }
             }
             float dg[32], du[32], aw[32];
@@ -507,9 +556,43 @@ __global__ void __launch_bounds__(192, 1)
               du[i] = da * pu;
               aw[i] = wrow * a;
             }
-            emit(&tmO0, dg, i0, ti.row0 + q * 32, 0, false);
-            emit(&tmO1, du, i0, ti.row0 + q * 32, 0, false);
-            emit(&tmO2, aw, i0, ti.row0 + q * 32, 0, false);
+            if constexpr (C::kTf32) {
+              // operands of the TF32 dgrad / wgrad products
+#pragma unroll
+              for (int i = 0; i < 32; ++i) {
+                dg[i] = round_tf32(dg[i]);
+                du[i] = round_tf32(du[i]);
+                aw[i] = round_tf32(aw[i]);
+              }
+              emit_tile<T, NBUF, C::OUT_TILE>(&maps.o[0], dg, i0, orow, 0, false, my_epi,
+                                              my_epi_s, buf, lane);
+              emit_tile<T, NBUF, C::OUT_TILE>(&maps.o[1], du, i0, orow, 0, false, my_epi,
+                                              my_epi_s, buf, lane);
+              emit_tile<T, NBUF, C::OUT_TILE>(&maps.o[2], aw, i0, orow, 0, false, my_epi,
+                                              my_epi_s, buf, lane);
+            } else {
+              // bf16 hi parts (operands of the dgrad and the wgrads) and lo
+              // parts (the remainders, operands of the wgrads only)
+              float lo[32];
+#pragma unroll
+              for (int i = 0; i < 32; ++i) split_bf16(dg[i], dg[i], lo[i]);
+              emit_tile<T, NBUF, C::OUT_TILE>(&maps.o[0], dg, i0, orow, 0, false, my_epi,
+                                              my_epi_s, buf, lane);
+              emit_tile<T, NBUF, C::OUT_TILE>(&maps.o[3], lo, i0, orow, 0, false, my_epi,
+                                              my_epi_s, buf, lane);
+#pragma unroll
+              for (int i = 0; i < 32; ++i) split_bf16(du[i], du[i], lo[i]);
+              emit_tile<T, NBUF, C::OUT_TILE>(&maps.o[1], du, i0, orow, 0, false, my_epi,
+                                              my_epi_s, buf, lane);
+              emit_tile<T, NBUF, C::OUT_TILE>(&maps.o[4], lo, i0, orow, 0, false, my_epi,
+                                              my_epi_s, buf, lane);
+#pragma unroll
+              for (int i = 0; i < 32; ++i) split_bf16(aw[i], aw[i], lo[i]);
+              emit_tile<T, NBUF, C::OUT_TILE>(&maps.o[2], aw, i0, orow, 0, false, my_epi,
+                                              my_epi_s, buf, lane);
+              emit_tile<T, NBUF, C::OUT_TILE>(&maps.o[5], lo, i0, orow, 0, false, my_epi,
+                                              my_epi_s, buf, lane);
+            }
           }
           args.dwpart[static_cast<int64_t>(ti.nt) * args.rows_max + row] = live ? dot : 0.f;
         }
@@ -532,7 +615,7 @@ __global__ void __launch_bounds__(192, 1)
 }
 
 template <typename T, int MODE, int BN, int STAGES, int NBUF>
-cudaError_t launch_gemm_t(const CUtensorMap* maps, const GemmArgs& args, int num_sms,
+cudaError_t launch_gemm_t(const GemmMaps& maps, const GemmArgs& args, int num_sms,
                           cudaStream_t st) {
   using C = GemmCfg<T, MODE, BN, STAGES, NBUF>;
   auto kern = moe_gemm_kernel<T, MODE, BN, STAGES, NBUF>;
@@ -545,8 +628,7 @@ cudaError_t launch_gemm_t(const CUtensorMap* maps, const GemmArgs& args, int num
     if (e != cudaSuccess) return e;
     configured[dev] = true;
   }
-  kern<<<num_sms, 192, C::SMEM_BYTES, st>>>(maps[0], maps[1], maps[2], maps[3], maps[4], maps[5],
-                                            args);
+  kern<<<num_sms, 192, C::SMEM_BYTES, st>>>(maps, args);
   return cudaGetLastError();
 }
 

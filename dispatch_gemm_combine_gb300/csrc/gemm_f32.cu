@@ -4,11 +4,11 @@
 
 namespace moe {
 
-cudaError_t launch_gemm_f32(int mode, const CUtensorMap* maps, const GemmArgs& a, int sms,
+cudaError_t launch_gemm_f32(int mode, const GemmMaps& maps, const GemmArgs& a, int sms,
                             cudaStream_t st) {
   using T = float;
   switch (mode) {
-    case kFwdGateUp: return launch_gemm_t<T, kFwdGateUp, 256, 3, 3>(maps, a, sms, st);
+    case kFwdGateUp: return launch_gemm_t<T, kFwdGateUp, 256, 3, 2>(maps, a, sms, st);
     case kFwdDown: return launch_gemm_t<T, kFwdDown, 256, 3, 2>(maps, a, sms, st);
     case kDgradDown: return launch_gemm_t<T, kDgradDown, 256, 3, 3>(maps, a, sms, st);
     case kDgradGateUp: return launch_gemm_t<T, kDgradGateUp, 256, 3, 2>(maps, a, sms, st);

@@ -18,17 +18,24 @@ size_t plan_blkhist_ints(int64_t Tk, int E);
 // ---- row movement (permute.cu); elem_bytes is 2 (bf16) or 4 (fp32)
 // dst[p] = src[perm[offsets[e] + p - poff[e]] / k] for the live rows of the
 // tile-padded expert-grouped layout; padding rows (and rows whose slot is
-// outside [0, tk)) are zero-filled.
+// outside [0, tk)) are zero-filled.  fp32 rows are rounded to TF32 (they are
+// TF32 tensor-core operands).
 cudaError_t launch_gather_rows(const void* src, int H, int k, int E, const int* poff,
                                const int* counts, const int* offsets, const int* perm, int tk,
                                int64_t rows_max, void* dst, int elem_bytes, int num_sms,
                                cudaStream_t st);
-// out[t] = sum_{j<k} src[row(t*k+j)] in fp32, j ascending; k <= 32.  A slot
-// with an out-of-range expert id contributes nothing.
-cudaError_t launch_combine(const void* src, int H, int k, int E, const int* idx, const int* inv,
+// out[t] = sum_{j<k} src[row(t*k+j)] in fp32, j ascending; k <= 32.  src
+// holds fp32 rows [rows_max, H]; out is [T, H] of 2- or 4-byte elements.  A
+// slot with an out-of-range expert id contributes nothing.
+cudaError_t launch_combine(const float* src, int H, int k, int E, const int* idx, const int* inv,
                            const int* offsets, const int* poff, int64_t T, int64_t rows_max,
-                           void* out,
-                           int elem_bytes, int num_sms, cudaStream_t st);
+                           void* out, int out_bytes, int num_sms, cudaStream_t st);
+// out[b][c][r] = round_tf32(in[b][r][c]) for fp32 [batch, rows, cols] arrays.
+cudaError_t launch_transpose_f32(const float* in, float* out, int batch, int rows, int cols,
+                                 cudaStream_t st);
+// out[i] = round_tf32(in[i]), n a multiple of 4.
+cudaError_t launch_round_copy_tf32(const float* in, float* out, int64_t n, int num_sms,
+                                   cudaStream_t st);
 // d_topk_w[s] = sum_{n < ntiles} dwpart[n * rows_max + row(s)], n ascending.
 cudaError_t launch_dw_reduce(const float* dwpart, int ntiles, int64_t rows_max, int E,
                              const int* idx,
@@ -68,8 +75,15 @@ struct GemmArgs {
   uint64_t timeout_ns;
 };
 
-// maps: A, B0, B1, O0, O1, O2 (unused ones may repeat a valid map).
-cudaError_t launch_gemm(int mode, int elem_bytes, const CUtensorMap* maps, const GemmArgs& args,
+// TMA descriptors of one GEMM launch (unused ones may repeat a valid map):
+//   a   A operand (hi part when split)      a2  A lo part (split A)
+//   b0  B operand (hi part / gate view)     b1  B lo part (split B) / up view
+//   o   outputs, mode-specific (see the epilogue).
+struct GemmMaps {
+  CUtensorMap a, a2, b0, b1, o[6];
+};
+
+cudaError_t launch_gemm(int mode, int elem_bytes, const GemmMaps& maps, const GemmArgs& args,
                         int num_sms, cudaStream_t st);
 // Column tile width (N) of the output for a mode, as used by launch_gemm.
 int gemm_block_n(int mode, int elem_bytes);

@@ -2,7 +2,8 @@
 //   gather   ("sparse token extraction" / "each token is repeated k times")
 //   combine  (the accumulate-back step the dispatch-and-combine page does with
 //             index_add_; here a k-way gather-sum per token in a fixed order,
-//             so no float atomics and bitwise-reproducible results)
+//             so no float atomics and bitwise-reproducible results; its
+//             inputs are the fp32 rows the GEMM epilogues write)
 //   dw_reduce (fixed-order sum of the per-column-tile partial dot products
 //             that make d(topk weights))
 // All three are HBM-bound: one warp per row, 16-byte vector accesses,
@@ -41,7 +42,7 @@ __device__ __forceinline__ int64_t padded_row_of_slot(int s, int E, const int* _
 __global__ void __launch_bounds__(256) gather_rows_kernel(
     const uint4* __restrict__ src, int vec_per_row, int k, int E, const int* __restrict__ poff,
     const int* __restrict__ counts, const int* __restrict__ offsets, const int* __restrict__ perm,
-    int tk, int64_t rows_max, uint4* __restrict__ dst) {
+    int tk, int64_t rows_max, int tf32, uint4* __restrict__ dst) {
   const int lane = threadIdx.x & 31;
   const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
   // never past the workspace bound, even for an inconsistent caller plan
@@ -55,7 +56,17 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(
     const int slot = (local < __ldg(counts + e) && gi < tk) ? __ldg(perm + gi) : -1;
     if (slot >= 0 && slot < tk) {
       const uint4* sr = src + static_cast<int64_t>(slot / k) * vec_per_row;
-      for (int v = lane; v < vec_per_row; v += 32) d[v] = __ldg(sr + v);
+      if (tf32) {
+        for (int v = lane; v < vec_per_row; v += 32) {
+          const uint4 a = __ldg(sr + v);
+          d[v] = make_uint4(__float_as_uint(round_tf32(__uint_as_float(a.x))),
+                            __float_as_uint(round_tf32(__uint_as_float(a.y))),
+                            __float_as_uint(round_tf32(__uint_as_float(a.z))),
+                            __float_as_uint(round_tf32(__uint_as_float(a.w))));
+        }
+      } else {
+        for (int v = lane; v < vec_per_row; v += 32) d[v] = __ldg(sr + v);
+      }
     } else {
       const uint4 z = make_uint4(0, 0, 0, 0);
       for (int v = lane; v < vec_per_row; v += 32) d[v] = z;
@@ -63,73 +74,80 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(
   }
 }
 
-template <typename T>
-struct Vec8;  // 16 bytes of T
-template <>
-struct Vec8<__nv_bfloat16> {
-  static constexpr int N = 8;
-  __device__ static void add(float* acc, uint4 v) {
-    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const float2 f = __bfloat1622float2(h[i]);
-      acc[2 * i] += f.x;
-      acc[2 * i + 1] += f.y;
-    }
-  }
-  __device__ static uint4 pack(const float* acc) {
-    uint4 v;
-    __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&v);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) h[i] = __floats2bfloat162_rn(acc[2 * i], acc[2 * i + 1]);
-    return v;
-  }
-};
-template <>
-struct Vec8<float> {
-  static constexpr int N = 4;
-  __device__ static void add(float* acc, uint4 v) {
-    acc[0] += __uint_as_float(v.x);
-    acc[1] += __uint_as_float(v.y);
-    acc[2] += __uint_as_float(v.z);
-    acc[3] += __uint_as_float(v.w);
-  }
-  __device__ static uint4 pack(const float* acc) {
-    return make_uint4(__float_as_uint(acc[0]), __float_as_uint(acc[1]), __float_as_uint(acc[2]),
-                      __float_as_uint(acc[3]));
-  }
-};
-
 constexpr int kMaxK = 32;
 
-template <typename T>
-__global__ void __launch_bounds__(256) combine_kernel(const uint4* __restrict__ src,
-                                                      int vec_per_row, int k, int E,
-                                                      const int* __restrict__ idx,
+__device__ __forceinline__ void store8(__nv_bfloat16* out, const float* a) {
+  uint4 v;
+  __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&v);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) h[i] = __floats2bfloat162_rn(a[2 * i], a[2 * i + 1]);
+  *reinterpret_cast<uint4*>(out) = v;
+}
+__device__ __forceinline__ void store8(float* out, const float* a) {
+  reinterpret_cast<float4*>(out)[0] = make_float4(a[0], a[1], a[2], a[3]);
+  reinterpret_cast<float4*>(out)[1] = make_float4(a[4], a[5], a[6], a[7]);
+}
+
+// src: fp32 rows of the padded layout [rows_max, H]; out: [T, H] of OutT.
+// One warp per token, 8 columns per lane per step.
+template <typename OutT>
+__global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ src, int H, int k,
+                                                      int E, const int* __restrict__ idx,
                                                       const int* __restrict__ inv,
                                                       const int* __restrict__ offsets,
                                                       const int* __restrict__ poff, int64_t T_,
-                                                      int64_t rows_max, uint4* __restrict__ out) {
+                                                      int64_t rows_max, OutT* __restrict__ out) {
   __shared__ int64_t rows_s[8][kMaxK];   // padded rows of the current token's k slots
   const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
   const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+  const int groups = H / 8;
   for (int64_t t = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + wib; t < T_;
        t += warps) {
     if (lane < k)
       rows_s[wib][lane] =
           padded_row_of_slot(static_cast<int>(t * k + lane), E, idx, inv, offsets, poff);
     __syncwarp();
-    for (int v = lane; v < vec_per_row; v += 32) {
-      float acc[Vec8<T>::N];
+    for (int v = lane; v < groups; v += 32) {
+      float acc[8];
 #pragma unroll
-      for (int i = 0; i < Vec8<T>::N; ++i) acc[i] = 0.f;
+      for (int i = 0; i < 8; ++i) acc[i] = 0.f;
       for (int j = 0; j < k; ++j) {
         const int64_t r = rows_s[wib][j];
-        if (r >= 0 && r < rows_max) Vec8<T>::add(acc, __ldg(src + r * vec_per_row + v));
+        if (r >= 0 && r < rows_max) {
+          const float4* p = reinterpret_cast<const float4*>(src + r * H + v * 8);
+          const float4 a = __ldg(p), b = __ldg(p + 1);
+          acc[0] += a.x; acc[1] += a.y; acc[2] += a.z; acc[3] += a.w;
+          acc[4] += b.x; acc[5] += b.y; acc[6] += b.z; acc[7] += b.w;
+        }
       }
-      out[t * vec_per_row + v] = Vec8<T>::pack(acc);
+      store8(out + t * H + v * 8, acc);
     }
     __syncwarp();
+  }
+}
+
+// out[b][c][r] = tf32_round(in[b][r][c]) (fp32), 32x32 tiles through shared
+// memory: K-major TF32 operands for the fp32 path.
+__global__ void __launch_bounds__(256) transpose_f32_kernel(const float* __restrict__ in,
+                                                            float* __restrict__ out, int rows,
+                                                            int cols) {
+  __shared__ float tile[32][33];
+  const int64_t plane = static_cast<int64_t>(rows) * cols;
+  in += blockIdx.z * plane;
+  out += blockIdx.z * plane;
+  const int c0 = blockIdx.x * 32;
+  for (int r0 = blockIdx.y * 32; r0 < rows; r0 += gridDim.y * 32) {
+    for (int i = threadIdx.y; i < 32; i += 8) {
+      const int r = r0 + i, c = c0 + threadIdx.x;
+      if (r < rows && c < cols) tile[i][threadIdx.x] = in[static_cast<int64_t>(r) * cols + c];
+    }
+    __syncthreads();
+    for (int i = threadIdx.y; i < 32; i += 8) {
+      const int c = c0 + i, r = r0 + threadIdx.x;
+      if (r < rows && c < cols)
+        out[static_cast<int64_t>(c) * rows + r] = round_tf32(tile[threadIdx.x][i]);
+    }
+    __syncthreads();
   }
 }
 
@@ -164,25 +182,50 @@ cudaError_t launch_gather_rows(const void* src, int H, int k, int E, const int* 
   const int vec = H * elem_bytes / 16;
   gather_rows_kernel<<<grid_for(rows_max, num_sms), 256, 0, st>>>(
       static_cast<const uint4*>(src), vec, k, E, poff, counts, offsets, perm, tk, rows_max,
-      static_cast<uint4*>(dst));
+      elem_bytes == 4 ? 1 : 0, static_cast<uint4*>(dst));
   return cudaGetLastError();
 }
 
-cudaError_t launch_combine(const void* src, int H, int k, int E, const int* idx, const int* inv,
+cudaError_t launch_combine(const float* src, int H, int k, int E, const int* idx, const int* inv,
                            const int* offsets, const int* poff, int64_t T, int64_t rows_max,
-                           void* out,
-                           int elem_bytes, int num_sms, cudaStream_t st) {
+                           void* out, int out_bytes, int num_sms, cudaStream_t st) {
   if (T == 0) return cudaSuccess;
   if (k > kMaxK) return cudaErrorInvalidValue;
-  const int vec = H * elem_bytes / 16;
-  if (elem_bytes == 2)
+  if (out_bytes == 2)
     combine_kernel<__nv_bfloat16><<<grid_for(T, num_sms), 256, 0, st>>>(
-        static_cast<const uint4*>(src), vec, k, E, idx, inv, offsets, poff, T, rows_max,
-        static_cast<uint4*>(out));
+        src, H, k, E, idx, inv, offsets, poff, T, rows_max, static_cast<__nv_bfloat16*>(out));
   else
     combine_kernel<float><<<grid_for(T, num_sms), 256, 0, st>>>(
-        static_cast<const uint4*>(src), vec, k, E, idx, inv, offsets, poff, T, rows_max,
-        static_cast<uint4*>(out));
+        src, H, k, E, idx, inv, offsets, poff, T, rows_max, static_cast<float*>(out));
+  return cudaGetLastError();
+}
+
+__global__ void __launch_bounds__(256) round_copy_tf32_kernel(const float4* __restrict__ in,
+                                                              float4* __restrict__ out, int64_t n4) {
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n4;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const float4 a = __ldg(in + i);
+    out[i] = make_float4(round_tf32(a.x), round_tf32(a.y), round_tf32(a.z), round_tf32(a.w));
+  }
+}
+
+cudaError_t launch_round_copy_tf32(const float* in, float* out, int64_t n, int num_sms,
+                                   cudaStream_t st) {
+  const int64_t n4 = n / 4;
+  if (n4 == 0) return cudaSuccess;
+  int64_t blocks = (n4 + 255) / 256;
+  if (blocks > static_cast<int64_t>(num_sms) * 8) blocks = static_cast<int64_t>(num_sms) * 8;
+  round_copy_tf32_kernel<<<static_cast<int>(blocks), 256, 0, st>>>(
+      reinterpret_cast<const float4*>(in), reinterpret_cast<float4*>(out), n4);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_transpose_f32(const float* in, float* out, int batch, int rows, int cols,
+                                 cudaStream_t st) {
+  if (batch == 0 || rows == 0 || cols == 0) return cudaSuccess;
+  const int gy = (rows + 31) / 32 < 65535 ? (rows + 31) / 32 : 65535;
+  dim3 grid((cols + 31) / 32, gy, batch);
+  transpose_f32_kernel<<<grid, dim3(32, 8), 0, st>>>(in, out, rows, cols);
   return cudaGetLastError();
 }
 

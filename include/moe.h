@@ -101,9 +101,10 @@ typedef struct {
  * 2 moe_ffn_bwd.  Returns 0 for an invalid shape or `which`. */
 size_t moe_workspace_size(const moe_shape* shape, int which);
 
-/* Bytes of the context the training forward saves for the backward (the
- * gate_up pre-activations, in the library's expert-grouped, tile-padded row
- * order).  Returns 0 for an invalid shape. */
+/* Bytes of the context the training forward saves for the backward: the
+ * gate_up pre-activations in fp32 (whatever the dtype, so the backward sees
+ * the accumulator values, not a bf16 rounding of them), in the library's
+ * expert-grouped, tile-padded row order.  Returns 0 for an invalid shape. */
 size_t moe_saved_size(const moe_shape* shape);
 
 /* Build the dispatch plan of topk_idx [T,k] (int32, device).
@@ -156,6 +157,27 @@ uint64_t moe_set_wait_timeout_ns(uint64_t ns);
 
 /* Static description of a status code. */
 const char* moe_status_string(moe_status status);
+
+/* ---- measurement helpers (no counterpart in the pages; they serve the
+ * roofline accounting of the benchmark) ---- */
+
+/* Number of kernels (and memsets) this library has launched in this
+ * process, across all entry points and devices. */
+uint64_t moe_kernel_launch_count(void);
+
+/* Turn the per-kernel event timer on (on != 0) or off; returns the previous
+ * setting.  While on, each entry point records a pair of CUDA events on the
+ * caller's stream around every kernel it launches (host-side event objects
+ * only, no device memory).  Off by default. */
+int moe_profile_enable(int on);
+
+/* Wait for the recorded events, add up the elapsed time per kernel kind since
+ * the last read, write up to `n` kinds into total_ms[] / launches[] (either
+ * may be NULL), reset the sums and return the number of kinds. */
+int moe_profile_read(double* total_ms, uint64_t* launches, int n);
+
+/* Name of kernel kind `kind` (NULL if out of range). */
+const char* moe_profile_kernel_name(int kind);
 
 #ifdef __cplusplus
 }
