@@ -250,6 +250,9 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="target length of the oracle sample (cpu_baseline)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--experts", type=int, default=None,
+                    help="profiling case: use this many experts and scale the tokens so each "
+                         "expert keeps the workload's rows (not a bench line)")
     args = ap.parse_args()
 
     rank = int(os.environ.get("RANK", "0"))
@@ -273,6 +276,8 @@ def main():
     if world > 1:
         dist.init_process_group("nccl")
     r = synth.RECIPES[args.workload]
+    if args.experts:
+        r = r.scaled(E=args.experts, T=max(1, r.T * args.experts // r.E))
     case = synth.make_case(r, device="cuda")
     dt = MOE_BF16 if r.dtype == "bf16" else MOE_FP32
     run = LayerRunner(r.T, r.H, r.I, r.E, r.k, r.act, dt, r.limit, r.alpha)
