@@ -162,6 +162,17 @@ def moe_profile_read():
     return {moe_profile_kernel_name(i): (ms[i], cnt[i]) for i in range(min(k, n))}
 
 
+def moe_plan_noalloc(shape, topk_idx, plan, stream):
+    """moe_plan without a workspace, for callers that cannot allocate device
+    memory when they build a plan; its scratch is a fixed array inside the
+    library (see include/moe.h for the size limit and the sharing rules)."""
+    fn = lib().moe_plan_noalloc
+    fn.argtypes = [ctypes.POINTER(MoeShape), ctypes.c_void_p, ctypes.POINTER(MoePlan),
+                   ctypes.c_void_p]
+    fn.restype = ctypes.c_int
+    return fn(ctypes.byref(shape), topk_idx, ctypes.byref(plan), stream)
+
+
 # ---------------------------------------------------------------- torch helpers
 def Shape(T, H, I, E, k, act=MOE_ACT_SWIGLU, dtype=MOE_BF16, clamp_limit=7.0, alpha=1.702):
     return MoeShape(T, H, I, E, k, act, clamp_limit, alpha, dtype)

@@ -158,6 +158,33 @@ uint64_t moe_set_wait_timeout_ns(uint64_t ns);
 /* Static description of a status code. */
 const char* moe_status_string(moe_status status);
 
+/* moe_plan without a workspace.  The pages have no counterpart to this
+ * entry point; it exists for callers that cannot allocate device memory at
+ * the point where they need a dispatch plan: code running inside an
+ * allocator-free region (a memory pool that is already carved up, a
+ * latency-critical path where cudaMalloc's implicit synchronisation is not
+ * acceptable, a host runtime that owns all device memory and only hands out
+ * the tensors it manages).  The plan kernels' scratch (per-chunk expert
+ * histograms, tile-padded offsets, an error word) then lives in a fixed
+ * 1 MiB array inside this library's device image, present on every GPU that
+ * loads the library until the process exits.  This call allocates nothing.
+ *   - Arguments and outputs are those of moe_plan, minus the workspace; the
+ *     result is identical to moe_plan's.
+ *   - Size limit: ceil(T*k / 1024) * E <= 260992 (e.g. T*k <= 1,043,456 for
+ *     E = 256, T*k <= 260,096 for E = 1024); larger problems return
+ *     MOE_ERR_WORKSPACE without launching anything.
+ *   - The first call on a device resolves the device address of the array
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture.
+ *   - Every call on a device shares the one array and leaves its contents
+ *     behind; the call clears what must start at zero.  Calls whose kernels
+ *     may overlap on the GPU (different streams, or different host threads)
+ *     race on the array and corrupt each other's plans: serialise them.
+ *   - An expert id outside [0, E) is left out of the counts; with no error
+ *     word to read, a caller detects it as offsets[E] < T*k. */
+moe_status moe_plan_noalloc(const moe_shape* shape, const int32_t* topk_idx,
+                            const moe_plan_t* plan, moe_stream_t stream);
+
 /* ---- measurement helpers (no counterpart in the pages; they serve the
  * roofline accounting of the benchmark) ---- */
 
