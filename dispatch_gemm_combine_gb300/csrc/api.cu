@@ -188,10 +188,16 @@ bool map3d(CUtensorMap* m, int es, const void* base, uint64_t d0, uint64_t d1, u
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Output tiles of the epilogue: 32 x 32 elements, swizzled to match the
-// staging layout (64B rows for 16-bit, 128B rows for fp32).
-CUtensorMapSwizzle out_swizzle(int es) {
-  return es == 2 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B;
+// Epilogue output view: element (b, r, c) at p[b*bstride + r*ld + c],
+// written only for r < rows and c < cols.
+OutDesc out_view(const void* p, int64_t ld, int64_t rows, int64_t cols, int64_t bstride = 0) {
+  OutDesc o;
+  o.ptr = const_cast<void*>(p);
+  o.ld = ld;
+  o.bstride = bstride;
+  o.rows = static_cast<int>(rows);
+  o.cols = static_cast<int>(cols);
+  return o;
 }
 
 // ------------------------------------------------------------ shape & layout
@@ -456,13 +462,11 @@ moe_status moe_ffn_fwd(const moe_shape* s, const void* x, const int32_t* topk_id
 
   const uint32_t BK = 128 / es, CH = 128 / es;
   const auto SW = CU_TENSOR_MAP_SWIZZLE_128B;
-  const auto OSW = out_swizzle(es);
-  const auto OSW32 = out_swizzle(4);
   const char* wgu = static_cast<const char*>(w_gate_up);
 
   // gate_up GEMM + activation (+ fp32 pre-activations saved for the backward)
   GemmMaps m1;
-  bool ok = map2d(&m1.a, es, xp, H, R, H, BK, 128, SW) && map2d(&m1.o[0], es, aact, I, R, I, 32, 32, OSW);
+  bool ok = map2d(&m1.a, es, xp, H, R, H, BK, 128, SW);
   if (es == 2) {
     ok = ok && map3d(&m1.b0, es, wgu, I, H, E, 2ll * I, 2ll * I * H, CH, BK, SW) &&
          map3d(&m1.b1, es, wgu + static_cast<size_t>(I) * es, I, H, E, 2ll * I, 2ll * I * H, CH,
@@ -477,18 +481,14 @@ moe_status moe_ffn_fwd(const moe_shape* s, const void* x, const int32_t* topk_id
          map3d(&m1.b1, es, wguT + static_cast<size_t>(I) * H, H, I, E, H, 2ll * I * H, BK, 128,
                SW);
   }
-  if (ok && saved) {
-    ok = map2d(&m1.o[1], 4, saved, I, R, 2ll * I, 32, 32, OSW32) &&
-         map2d(&m1.o[2], 4, static_cast<char*>(saved) + static_cast<size_t>(I) * 4, I, R, 2ll * I,
-               32, 32, OSW32);
-  } else {
-    m1.o[1] = m1.o[0];
-    m1.o[2] = m1.o[0];
-  }
   if (!ok) return MOE_ERR_CUDA;
   m1.a2 = m1.a;
-  for (int i = 3; i < 6; ++i) m1.o[i] = m1.o[0];
   GemmArgs a1 = base_args(s, poff, counts, offsets, perm, topk_w, err);
+  a1.out[0] = out_view(aact, I, R, I);
+  if (saved) {
+    a1.out[1] = out_view(saved, 2ll * I, R, I);
+    a1.out[2] = out_view(static_cast<float*>(saved) + I, 2ll * I, R, I);
+  }
   a1.num_kb = (H + BK - 1) / BK;
   a1.n_tiles = (I + gemm_block_n(kFwdGateUp, es) - 1) / gemm_block_n(kFwdGateUp, es);
   a1.save_h1 = saved ? 1 : 0;
@@ -497,7 +497,7 @@ moe_status moe_ffn_fwd(const moe_shape* s, const void* x, const int32_t* topk_id
   // down GEMM * routing weight -> fp32 rows Ow
   float* ow = at<float>(ws, L.ow);
   GemmMaps m2;
-  ok = map2d(&m2.a, es, aact, I, R, I, BK, 128, SW) && map2d(&m2.o[0], 4, ow, H, R, H, 32, 32, OSW32);
+  ok = map2d(&m2.a, es, aact, I, R, I, BK, 128, SW);
   if (es == 2) {
     ok = ok && map3d(&m2.b0, es, w_down, H, I, E, H, static_cast<int64_t>(H) * I, CH, BK, SW);
   } else {
@@ -510,8 +510,8 @@ moe_status moe_ffn_fwd(const moe_shape* s, const void* x, const int32_t* topk_id
   if (!ok) return MOE_ERR_CUDA;
   m2.a2 = m2.a;
   m2.b1 = m2.b0;
-  for (int i = 1; i < 6; ++i) m2.o[i] = m2.o[0];
   GemmArgs a2 = base_args(s, poff, counts, offsets, perm, topk_w, err);
+  a2.out[0] = out_view(ow, H, R, H);
   a2.num_kb = (I + BK - 1) / BK;
   a2.n_tiles = (H + gemm_block_n(kFwdDown, es) - 1) / gemm_block_n(kFwdDown, es);
   MOE_CUDA(tracked(kKFwdDown, 1, st, [&] { return launch_gemm(kFwdDown, es, m2, a2, sms, st); }));
@@ -583,8 +583,6 @@ moe_status moe_ffn_bwd(const moe_shape* s, const void* dy, const void* x, const 
 
   const uint32_t BK = 128 / es, CH = 128 / es;
   const auto SW = CU_TENSOR_MAP_SWIZZLE_128B;
-  const auto OSW = out_swizzle(es);
-  const auto OSW32 = out_swizzle(4);
   const size_t up_off = static_cast<size_t>(I) * es;
   bool ok;
 
@@ -609,13 +607,7 @@ moe_status moe_ffn_bwd(const moe_shape* s, const void* dy, const void* x, const 
   // (1) down dgrad + activation backward -> dH1 (gate | up), w*a, dw partials
   GemmMaps m1;
   ok = map2d(&m1.a, es, dyp, H, R, H, BK, 128, SW) &&
-       map3d(&m1.b0, es, wd_op, H, I, E, H, static_cast<int64_t>(H) * I, BK, 256, SW) &&
-       map2d(&m1.o[0], es, dh1, I, R, 2ll * I, 32, 32, OSW) &&
-       map2d(&m1.o[1], es, static_cast<char*>(dh1) + up_off, I, R, 2ll * I, 32, 32, OSW) &&
-       map2d(&m1.o[2], es, aw, I, R, I, 32, 32, OSW) &&
-       map2d(&m1.o[3], es, dh1lo, I, R, 2ll * I, 32, 32, OSW) &&
-       map2d(&m1.o[4], es, static_cast<char*>(dh1lo) + up_off, I, R, 2ll * I, 32, 32, OSW) &&
-       map2d(&m1.o[5], es, awlo, I, R, I, 32, 32, OSW);
+       map3d(&m1.b0, es, wd_op, H, I, E, H, static_cast<int64_t>(H) * I, BK, 256, SW);
   if (!ok) return MOE_ERR_CUDA;
   m1.a2 = m1.a;
   m1.b1 = m1.b0;
@@ -624,6 +616,12 @@ moe_status moe_ffn_bwd(const moe_shape* s, const void* dy, const void* x, const 
   a1.n_tiles = dgrad_down_ntiles(s);
   a1.h1 = saved;
   a1.dwpart = dwpart;
+  a1.out[0] = out_view(dh1, 2ll * I, R, I);
+  a1.out[1] = out_view(static_cast<char*>(dh1) + up_off, 2ll * I, R, I);
+  a1.out[2] = out_view(aw, I, R, I);
+  a1.out[3] = out_view(dh1lo, 2ll * I, R, I);
+  a1.out[4] = out_view(static_cast<char*>(dh1lo) + up_off, 2ll * I, R, I);
+  a1.out[5] = out_view(awlo, I, R, I);
   MOE_CUDA(tracked(kKDgradDown, 1, st, [&] { return launch_gemm(kDgradDown, es, m1, a1, sms, st); }));
   MOE_CUDA(tracked(kKDwReduce, 1, st, [&] {
     return launch_dw_reduce(dwpart, a1.n_tiles, R, E, topk_idx, inv, offsets, poff, Tk, d_topk_w,
@@ -632,9 +630,9 @@ moe_status moe_ffn_bwd(const moe_shape* s, const void* dy, const void* x, const 
 
   // (2) down wgrad: dWd[e] = (w*a)_e^T dYp_e  (w*a as a bf16 hi/lo pair)
   GemmMaps m2;
-  ok = map3d(&m2.o[0], 4, dw_down, H, I, E, H, static_cast<int64_t>(H) * I, 32, 32, OSW32);
+  ok = true;
   if (split) {
-    ok = ok && map2d(&m2.a, es, aw, I, R, I, CH, BK, SW) &&
+    ok = map2d(&m2.a, es, aw, I, R, I, CH, BK, SW) &&
          map2d(&m2.a2, es, awlo, I, R, I, CH, BK, SW) && map2d(&m2.b0, es, dyp, H, R, H, CH, BK, SW);
   } else {
     // TF32: K-major copies [I, R] and [H, R] of the row-major activations
@@ -651,8 +649,8 @@ moe_status moe_ffn_bwd(const moe_shape* s, const void* dy, const void* x, const 
   }
   if (!ok) return MOE_ERR_CUDA;
   m2.b1 = m2.b0;
-  for (int i = 1; i < 6; ++i) m2.o[i] = m2.o[0];
   GemmArgs a2 = base_args(s, poff, counts, offsets, perm, topk_w, err);
+  a2.out[0] = out_view(dw_down, H, I, H, static_cast<int64_t>(I) * H);
   a2.m_tiles = (I + 127) / 128;
   a2.n_tiles = (H + gemm_block_n(kWgradDown, es) - 1) / gemm_block_n(kWgradDown, es);
   MOE_CUDA(tracked(kKWgradDown, 1, st, [&] { return launch_gemm(kWgradDown, es, m2, a2, sms, st); }));
@@ -661,13 +659,12 @@ moe_status moe_ffn_bwd(const moe_shape* s, const void* dy, const void* x, const 
   float* dxp = at<float>(ws, L.dxp);
   GemmMaps m3;
   ok = map2d(&m3.a, es, dh1, 2ll * I, R, 2ll * I, BK, 128, SW) &&
-       map3d(&m3.b0, es, wgu_op, 2ll * I, H, E, 2ll * I, 2ll * I * H, BK, 256, SW) &&
-       map2d(&m3.o[0], 4, dxp, H, R, H, 32, 32, OSW32);
+       map3d(&m3.b0, es, wgu_op, 2ll * I, H, E, 2ll * I, 2ll * I * H, BK, 256, SW);
   if (!ok) return MOE_ERR_CUDA;
   m3.a2 = m3.a;
   m3.b1 = m3.b0;
-  for (int i = 1; i < 6; ++i) m3.o[i] = m3.o[0];
   GemmArgs a3 = base_args(s, poff, counts, offsets, perm, topk_w, err);
+  a3.out[0] = out_view(dxp, H, R, H);
   a3.num_kb = (2 * I + BK - 1) / BK;
   a3.n_tiles = (H + gemm_block_n(kDgradGateUp, es) - 1) / gemm_block_n(kDgradGateUp, es);
   MOE_CUDA(tracked(kKDgradGateUp, 1, st, [&] { return launch_gemm(kDgradGateUp, es, m3, a3, sms, st); }));
@@ -678,9 +675,9 @@ moe_status moe_ffn_bwd(const moe_shape* s, const void* dy, const void* x, const 
   // (4) gate_up wgrad: dWgu[e] = Xp_e^T dH1_e  (dH1 as a bf16 hi/lo pair)
   const int bn4 = gemm_block_n(kWgradGateUp, es);
   GemmMaps m4;
-  ok = map3d(&m4.o[0], 4, dw_gate_up, 2ll * I, H, E, 2ll * I, 2ll * I * H, 32, 32, OSW32);
+  ok = true;
   if (split) {
-    ok = ok && map2d(&m4.a, es, xp, H, R, H, CH, BK, SW) &&
+    ok = map2d(&m4.a, es, xp, H, R, H, CH, BK, SW) &&
          map2d(&m4.b0, es, dh1, 2ll * I, R, 2ll * I, CH, BK, SW) &&
          map2d(&m4.b1, es, dh1lo, 2ll * I, R, 2ll * I, CH, BK, SW);
   } else {
@@ -697,8 +694,8 @@ moe_status moe_ffn_bwd(const moe_shape* s, const void* dy, const void* x, const 
   }
   if (!ok) return MOE_ERR_CUDA;
   m4.a2 = m4.a;
-  for (int i = 1; i < 6; ++i) m4.o[i] = m4.o[0];
   GemmArgs a4 = base_args(s, poff, counts, offsets, perm, topk_w, err);
+  a4.out[0] = out_view(dw_gate_up, 2ll * I, H, 2ll * I, 2ll * I * H);
   a4.m_tiles = (H + 127) / 128;
   a4.n_tiles = (2 * I + bn4 - 1) / bn4;
   MOE_CUDA(tracked(kKWgradGateUp, 1, st, [&] { return launch_gemm(kWgradGateUp, es, m4, a4, sms, st); }));

@@ -33,7 +33,7 @@ namespace moe {
 // that a CTA never exits with asynchronous work still writing its memory.
 constexpr uint64_t kDrainNs = 1000000000ull;
 
-template <typename T, int MODE, int BN, int STAGES, int NBUF>
+template <typename T, int MODE, int BN, int STAGES>
 struct GemmCfg {
   static constexpr int kES = sizeof(T);
   static constexpr bool kTf32 = (kES == 4);
@@ -58,13 +58,9 @@ struct GemmCfg {
   static constexpr int B_BYTES = B_PART * (SPLIT_B ? 2 : 1);
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int CHUNK_BYTES = BK * 128;   // one MN-major box
-  // 32x32 output staging tile: fp32 outputs (weight gradients, the saved
-  // fp32 pre-activations, the fp32 rows the combine sums, or fp32 storage)
-  // take 4 KB, 16-bit ones 2 KB.
-  static constexpr bool kOut32 =
-      kWgrad || kTf32 || MODE == kFwdGateUp || MODE == kFwdDown || MODE == kDgradGateUp;
-  static constexpr int OUT_TILE = 32 * 32 * (kOut32 ? 4 : 2);
-  static constexpr int EPI_BYTES = 4 * NBUF * OUT_TILE;
+  // per epilogue warp: one 32x32 transpose tile, rows padded to 36 words
+  static constexpr int EPI_WARP_BYTES = 32 * 36 * 4;
+  static constexpr int EPI_BYTES = 4 * EPI_WARP_BYTES;
   static constexpr int BAR_BYTES = (2 * STAGES + 5) * 8 + 16;
   static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + EPI_BYTES + BAR_BYTES;
   static constexpr int TMEM_COLS = (2 * BN <= 256) ? 256 : 512;
@@ -151,56 +147,59 @@ __device__ __forceinline__ void act_bwd(int act, float g, float u, float L, floa
   }
 }
 
-// Write 32 values (this thread's row of a 32x32 output tile) into a staging
-// tile in the swizzled layout the TMA store expects: 64-byte rows with the
-// 64B swizzle for 16-bit outputs, 128-byte rows with the 128B swizzle for
-// fp32 outputs.  The 16-byte unit j of row r sits at unit j ^ f(r), so the
-// 32 lanes of a warp (one row each) spread over all banks.
+// Store this warp's 32x32 output tile: lane i holds row r0+i, columns
+// [c0, c0+32).  The tile goes through a per-warp shared-memory transpose
+// (rows padded so that both the row-wise writes and the column-wise reads
+// are free of bank conflicts), then every store instruction writes whole
+// rows: 8 lanes x 16 B = one 128-byte fp32 row segment, or 4 lanes x 16 B =
+// one 64-byte bf16 row segment.  Rows >= o.rows and columns >= o.cols are
+// not written.
 template <typename O>
-__device__ __forceinline__ void stage_row(uint8_t* buf, int lane, const float (&v)[32]) {
-  if constexpr (sizeof(O) == 2) {
-    uint8_t* row = buf + lane * 64;
-    const int x = (lane >> 1) & 3;
+__device__ __forceinline__ void store_tile(const OutDesc& o, int b, int r0, int c0,
+                                           const float (&v)[32], uint8_t* stage, int lane) {
+  O* base = static_cast<O*>(o.ptr) + static_cast<int64_t>(b) * o.bstride;
+  if constexpr (sizeof(O) == 4) {
+    float* st = reinterpret_cast<float*>(stage);
+    float* row = st + lane * 36;
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      *reinterpret_cast<float4*>(row + 4 * j) =
+          make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+    __syncwarp();
+    const int c = (lane & 7) * 4;
+#pragma unroll
+    for (int it = 0; it < 8; ++it) {
+      const int r = it * 4 + (lane >> 3);
+      const float4 val = *reinterpret_cast<const float4*>(st + r * 36 + c);
+      const int gr = r0 + r, gc = c0 + c;
+      if (gr < o.rows && gc < o.cols)
+        *reinterpret_cast<float4*>(base + static_cast<int64_t>(gr) * o.ld + gc) = val;
+    }
+    __syncwarp();
+  } else {
+    __nv_bfloat16* st = reinterpret_cast<__nv_bfloat16*>(stage);
+    __nv_bfloat16* row = st + lane * 40;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       uint4 pk;
       __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&pk);
 #pragma unroll
       for (int i = 0; i < 4; ++i) h[i] = __floats2bfloat162_rn(v[8 * j + 2 * i], v[8 * j + 2 * i + 1]);
-      *reinterpret_cast<uint4*>(row + ((j ^ x) << 4)) = pk;
+      *reinterpret_cast<uint4*>(row + 8 * j) = pk;
     }
-  } else {
-    uint8_t* row = buf + lane * 128;
-    const int x = lane & 7;
+    __syncwarp();
+    const int c = (lane & 3) * 8;
 #pragma unroll
-    for (int j = 0; j < 8; ++j)
-      *reinterpret_cast<uint4*>(row + ((j ^ x) << 4)) =
-          make_uint4(__float_as_uint(v[4 * j]), __float_as_uint(v[4 * j + 1]),
-                     __float_as_uint(v[4 * j + 2]), __float_as_uint(v[4 * j + 3]));
+    for (int it = 0; it < 4; ++it) {
+      const int r = it * 8 + (lane >> 2);
+      const uint4 val = *reinterpret_cast<const uint4*>(st + r * 40 + c);
+      const int gr = r0 + r, gc = c0 + c;
+      if (gr < o.rows && gc < o.cols)
+        *reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(base) +
+                                  static_cast<int64_t>(gr) * o.ld + gc) = val;
+    }
+    __syncwarp();
   }
-}
-
-// Stage one 32x32 output tile (this thread's row) and store it with TMA;
-// `buf` cycles through NBUF staging buffers of this warp.
-template <typename O, int NBUF, int OUT_TILE>
-__device__ __forceinline__ void emit_tile(const CUtensorMap* map, const float (&v)[32], int c0,
-                                          int c1, int c2, bool three_d, uint8_t* my_epi,
-                                          uint32_t my_epi_s, int& buf, int lane) {
-  if (lane == 0) bulk_wait_read<NBUF - 1>();
-  __syncwarp();
-  stage_row<O>(my_epi + buf * OUT_TILE, lane, v);
-  fence_async_shared();
-  __syncwarp();
-  if (lane == 0) {
-    const uint32_t bs = my_epi_s + buf * OUT_TILE;
-    if (three_d)
-      tma_store_3d(map, bs, c0, c1, c2);
-    else
-      tma_store_2d(map, bs, c0, c1);
-    bulk_commit();
-  }
-  __syncwarp();
-  if (++buf == NBUF) buf = 0;
 }
 
 __device__ __forceinline__ void split_bf16(float x, float& hi, float& lo) {
@@ -208,10 +207,10 @@ __device__ __forceinline__ void split_bf16(float x, float& hi, float& lo) {
   lo = x - hi;
 }
 
-template <typename T, int MODE, int BN, int STAGES, int NBUF>
+template <typename T, int MODE, int BN, int STAGES>
 __global__ void __launch_bounds__(192, 1)
-    moe_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs args) {
-  using C = GemmCfg<T, MODE, BN, STAGES, NBUF>;
+    moe_gemm_kernel(const __grid_constant__ GemmMaps maps, const __grid_constant__ GemmArgs args) {
+  using C = GemmCfg<T, MODE, BN, STAGES>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t sbase = (raw + 1023u) & ~1023u;
@@ -437,9 +436,7 @@ __global__ void __launch_bounds__(192, 1)
   } else {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;                 // TMEM lane quarter = tile rows q*32..q*32+31
-    uint8_t* my_epi = epi_g + (warp - 2) * NBUF * C::OUT_TILE;
-    const uint32_t my_epi_s = smem_u32(my_epi);
-    int buf = 0;
+    uint8_t* my_epi = epi_g + (warp - 2) * C::EPI_WARP_BYTES;
     int acc = 0;
     uint32_t acc_phase = 0;
 
@@ -467,8 +464,7 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
             for (int i = 0; i < 32; ++i) v[i] = 0.f;
           }
-          emit_tile<float, NBUF, C::OUT_TILE>(&maps.o[0], v, ti.n0 + c * 32, ti.m0 + q * 32, ti.e,
-                                              true, my_epi, my_epi_s, buf, lane);
+          store_tile<float>(args.out[0], ti.e, ti.m0 + q * 32, ti.n0 + c * 32, v, my_epi, lane);
         }
       } else {
         // routing weight and liveness of this thread's row
@@ -489,18 +485,15 @@ __global__ void __launch_bounds__(192, 1)
             tmem_ld32(tacc + c * 32, v);
             tmem_ld32(tacc + BN / 2 + c * 32, u);
             if (args.save_h1) {
-              emit_tile<float, NBUF, C::OUT_TILE>(&maps.o[1], v, ti.n0 + c * 32, orow, 0, false,
-                                                  my_epi, my_epi_s, buf, lane);
-              emit_tile<float, NBUF, C::OUT_TILE>(&maps.o[2], u, ti.n0 + c * 32, orow, 0, false,
-                                                  my_epi, my_epi_s, buf, lane);
+              store_tile<float>(args.out[1], 0, orow, ti.n0 + c * 32, v, my_epi, lane);
+              store_tile<float>(args.out[2], 0, orow, ti.n0 + c * 32, u, my_epi, lane);
             }
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
               v[i] = act_fwd<T>(args.act, v[i], u[i], args.limit, args.alpha);
               if constexpr (C::kTf32) v[i] = round_tf32(v[i]);   // operand of the down GEMM
             }
-            emit_tile<T, NBUF, C::OUT_TILE>(&maps.o[0], v, ti.n0 + c * 32, orow, 0, false, my_epi,
-                                            my_epi_s, buf, lane);
+            store_tile<T>(args.out[0], 0, orow, ti.n0 + c * 32, v, my_epi, lane);
           }
         } else if constexpr (MODE == kFwdDown) {
 #pragma unroll 1
@@ -508,15 +501,13 @@ __global__ void __launch_bounds__(192, 1)
             tmem_ld32(tacc + c * 32, v);
 #pragma unroll
             for (int i = 0; i < 32; ++i) v[i] *= wrow;
-            emit_tile<float, NBUF, C::OUT_TILE>(&maps.o[0], v, ti.n0 + c * 32, orow, 0, false,
-                                                my_epi, my_epi_s, buf, lane);
+            store_tile<float>(args.out[0], 0, orow, ti.n0 + c * 32, v, my_epi, lane);
           }
         } else if constexpr (MODE == kDgradGateUp) {
 #pragma unroll 1
           for (int c = 0; c < BN / 32; ++c) {
             tmem_ld32(tacc + c * 32, v);
-            emit_tile<float, NBUF, C::OUT_TILE>(&maps.o[0], v, ti.n0 + c * 32, orow, 0, false,
-                                                my_epi, my_epi_s, buf, lane);
+            store_tile<float>(args.out[0], 0, orow, ti.n0 + c * 32, v, my_epi, lane);
           }
         } else {  // kDgradDown
           // saved fp32 pre-activations of this row: gate at [0, I), up at [I, 2I)
@@ -564,34 +555,25 @@ __global__ void __launch_bounds__(192, 1)
                 du[i] = round_tf32(du[i]);
                 aw[i] = round_tf32(aw[i]);
               }
-              emit_tile<T, NBUF, C::OUT_TILE>(&maps.o[0], dg, i0, orow, 0, false, my_epi,
-                                              my_epi_s, buf, lane);
-              emit_tile<T, NBUF, C::OUT_TILE>(&maps.o[1], du, i0, orow, 0, false, my_epi,
-                                              my_epi_s, buf, lane);
-              emit_tile<T, NBUF, C::OUT_TILE>(&maps.o[2], aw, i0, orow, 0, false, my_epi,
-                                              my_epi_s, buf, lane);
+              store_tile<T>(args.out[0], 0, orow, i0, dg, my_epi, lane);
+              store_tile<T>(args.out[1], 0, orow, i0, du, my_epi, lane);
+              store_tile<T>(args.out[2], 0, orow, i0, aw, my_epi, lane);
             } else {
               // bf16 hi parts (operands of the dgrad and the wgrads) and lo
               // parts (the remainders, operands of the wgrads only)
               float lo[32];
 #pragma unroll
               for (int i = 0; i < 32; ++i) split_bf16(dg[i], dg[i], lo[i]);
-              emit_tile<T, NBUF, C::OUT_TILE>(&maps.o[0], dg, i0, orow, 0, false, my_epi,
-                                              my_epi_s, buf, lane);
-              emit_tile<T, NBUF, C::OUT_TILE>(&maps.o[3], lo, i0, orow, 0, false, my_epi,
-                                              my_epi_s, buf, lane);
+              store_tile<T>(args.out[0], 0, orow, i0, dg, my_epi, lane);
+              store_tile<T>(args.out[3], 0, orow, i0, lo, my_epi, lane);
 #pragma unroll
               for (int i = 0; i < 32; ++i) split_bf16(du[i], du[i], lo[i]);
-              emit_tile<T, NBUF, C::OUT_TILE>(&maps.o[1], du, i0, orow, 0, false, my_epi,
-                                              my_epi_s, buf, lane);
-              emit_tile<T, NBUF, C::OUT_TILE>(&maps.o[4], lo, i0, orow, 0, false, my_epi,
-                                              my_epi_s, buf, lane);
+              store_tile<T>(args.out[1], 0, orow, i0, du, my_epi, lane);
+              store_tile<T>(args.out[4], 0, orow, i0, lo, my_epi, lane);
 #pragma unroll
               for (int i = 0; i < 32; ++i) split_bf16(aw[i], aw[i], lo[i]);
-              emit_tile<T, NBUF, C::OUT_TILE>(&maps.o[2], aw, i0, orow, 0, false, my_epi,
-                                              my_epi_s, buf, lane);
-              emit_tile<T, NBUF, C::OUT_TILE>(&maps.o[5], lo, i0, orow, 0, false, my_epi,
-                                              my_epi_s, buf, lane);
+              store_tile<T>(args.out[2], 0, orow, i0, aw, my_epi, lane);
+              store_tile<T>(args.out[5], 0, orow, i0, lo, my_epi, lane);
             }
           }
           args.dwpart[static_cast<int64_t>(ti.nt) * args.rows_max + row] = live ? dot : 0.f;
@@ -604,8 +586,6 @@ __global__ void __launch_bounds__(192, 1)
         acc_phase ^= 1u;
       }
     }
-    if (lane == 0) bulk_wait_all();
-    __syncwarp();
   }
 
   tc_fence_before();
@@ -614,11 +594,11 @@ __global__ void __launch_bounds__(192, 1)
   if (warp == 1) tmem_dealloc(tmem_base, C::TMEM_COLS);
 }
 
-template <typename T, int MODE, int BN, int STAGES, int NBUF>
+template <typename T, int MODE, int BN, int STAGES>
 cudaError_t launch_gemm_t(const GemmMaps& maps, const GemmArgs& args, int num_sms,
                           cudaStream_t st) {
-  using C = GemmCfg<T, MODE, BN, STAGES, NBUF>;
-  auto kern = moe_gemm_kernel<T, MODE, BN, STAGES, NBUF>;
+  using C = GemmCfg<T, MODE, BN, STAGES>;
+  auto kern = moe_gemm_kernel<T, MODE, BN, STAGES>;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;

@@ -52,6 +52,16 @@ enum GemmMode : int {
   kWgradGateUp = 5   // dWgu[e] = Xp^T dH1
 };
 
+// One epilogue output: element (b, r, c) lives at ptr[b*bstride + r*ld + c];
+// rows >= rows and columns >= cols are not written.
+struct OutDesc {
+  void* ptr;
+  int64_t ld;
+  int64_t bstride;
+  int rows;
+  int cols;
+};
+
 struct GemmArgs {
   const int* poff;      // [E+1] tile-padded row offsets
   const int* counts;    // [E]
@@ -73,14 +83,15 @@ struct GemmArgs {
   int64_t rows_max;
   int* err;
   uint64_t timeout_ns;
+  OutDesc out[6];       // mode-specific outputs (see the epilogue)
 };
 
-// TMA descriptors of one GEMM launch (unused ones may repeat a valid map):
+// TMA descriptors of the operands of one GEMM launch (unused ones may repeat
+// a valid map):
 //   a   A operand (hi part when split)      a2  A lo part (split A)
 //   b0  B operand (hi part / gate view)     b1  B lo part (split B) / up view
-//   o   outputs, mode-specific (see the epilogue).
 struct GemmMaps {
-  CUtensorMap a, a2, b0, b1, o[6];
+  CUtensorMap a, a2, b0, b1;
 };
 
 cudaError_t launch_gemm(int mode, int elem_bytes, const GemmMaps& maps, const GemmArgs& args,
