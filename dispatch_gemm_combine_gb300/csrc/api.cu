@@ -47,6 +47,12 @@ int gemm_block_n(int mode, int elem_bytes) {
   return 256;
 }
 
+// Output rows per weight-gradient tile (two 128-row m-tiles for the bf16
+// gate_up weight gradient).
+int gemm_block_m(int mode, int elem_bytes) {
+  return (mode == kWgradGateUp && elem_bytes == 2) ? 256 : 128;
+}
+
 }  // namespace moe
 
 using namespace moe;
@@ -696,7 +702,7 @@ moe_status moe_ffn_bwd(const moe_shape* s, const void* dy, const void* x, const 
   m4.a2 = m4.a;
   GemmArgs a4 = base_args(s, poff, counts, offsets, perm, topk_w, err);
   a4.out[0] = out_view(dw_gate_up, 2ll * I, H, 2ll * I, 2ll * I * H);
-  a4.m_tiles = (H + 127) / 128;
+  a4.m_tiles = (H + gemm_block_m(kWgradGateUp, es) - 1) / gemm_block_m(kWgradGateUp, es);
   a4.n_tiles = (2 * I + bn4 - 1) / bn4;
   MOE_CUDA(tracked(kKWgradGateUp, 1, st, [&] { return launch_gemm(kWgradGateUp, es, m4, a4, sms, st); }));
   return MOE_OK;

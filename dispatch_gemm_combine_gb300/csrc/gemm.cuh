@@ -52,18 +52,26 @@ struct GemmCfg {
   // accumulator (about 16 bits of mantissa instead of 8).
   static constexpr bool SPLIT_A = (MODE == kWgradDown) && !kTf32;
   static constexpr bool SPLIT_B = (MODE == kWgradGateUp) && !kTf32;
+  // m-tiles of 128 rows per CTA tile: the gate_up weight gradient computes
+  // two, so its (split, hence doubled) B tile is loaded once for both.
+  static constexpr int MT = (MODE == kWgradGateUp && !kTf32) ? 2 : 1;
   static constexpr int A_PART = BM * 128;
   static constexpr int B_PART = BN * 128;
-  static constexpr int A_BYTES = A_PART * (SPLIT_A ? 2 : 1);
+  static constexpr int A_BYTES = A_PART * MT * (SPLIT_A ? 2 : 1);
   static constexpr int B_BYTES = B_PART * (SPLIT_B ? 2 : 1);
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int CHUNK_BYTES = BK * 128;   // one MN-major box
-  // per epilogue warp: one 32x32 transpose tile, rows padded to 36 words
+  // per epilogue warp: one 32x32 transpose tile, rows padded to 36 words;
+  // the down dgrad also stages the saved pre-activations of its 32 rows
+  // (32 gate + 32 up fp32 per row, rows padded to 68 words)
   static constexpr int EPI_WARP_BYTES = 32 * 36 * 4;
-  static constexpr int EPI_BYTES = 4 * EPI_WARP_BYTES;
+  static constexpr int H1_WARP_BYTES = (MODE == kDgradDown) ? 32 * 68 * 4 : 0;
+  static constexpr int EPI_BYTES = 4 * (EPI_WARP_BYTES + H1_WARP_BYTES);
   static constexpr int BAR_BYTES = (2 * STAGES + 5) * 8 + 16;
   static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + EPI_BYTES + BAR_BYTES;
-  static constexpr int TMEM_COLS = (2 * BN <= 256) ? 256 : 512;
+  static constexpr int ACC_COLS = MT * BN;   // TMEM columns of one tile's accumulator(s)
+  static constexpr int TMEM_COLS = (2 * ACC_COLS <= 256) ? 256 : 512;
+  static_assert(2 * ACC_COLS <= 512, "two accumulators must fit in tensor memory");
   // output columns produced per tile (gate_up: BN/2 gate + BN/2 up -> BN/2)
   static constexpr int BN_OUT = (MODE == kFwdGateUp) ? BN / 2 : BN;
   static constexpr uint32_t IDESC = make_idesc(kTf32, A_MN, B_MN, BM, BN);
@@ -81,7 +89,7 @@ struct TileInfo {
   int nt;      // column-tile index
 };
 
-template <int BN_OUT, bool kWgrad>
+template <int BN_OUT, bool kWgrad, int MT = 1>
 __device__ __forceinline__ TileInfo decode_tile(const GemmArgs& a, int t, int bk) {
   TileInfo ti;
   if constexpr (kWgrad) {
@@ -90,7 +98,7 @@ __device__ __forceinline__ TileInfo decode_tile(const GemmArgs& a, int t, int bk
     const int r = t - ti.e * per_e;
     const int m = r / a.n_tiles;
     ti.nt = r - m * a.n_tiles;
-    ti.m0 = m * 128;
+    ti.m0 = m * 128 * MT;
     ti.n0 = ti.nt * BN_OUT;
     ti.row0 = __ldg(a.poff + ti.e);
     ti.nkb = (__ldg(a.poff + ti.e + 1) - ti.row0) / bk;
@@ -270,7 +278,7 @@ __global__ void __launch_bounds__(192, 1)
     int64_t issued = 0;
     bool ok = true;
     for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-      const TileInfo ti = decode_tile<C::BN_OUT, C::kWgrad>(args, t, C::BK);
+      const TileInfo ti = decode_tile<C::BN_OUT, C::kWgrad, C::MT>(args, t, C::BK);
       for (int kb = 0; kb < ti.nkb; ++kb) {
         int good = 1;
         if (lane == 0) good = mbar_wait(empty_bar + 8 * stage, phase ^ 1u, tmo);
@@ -316,6 +324,12 @@ __global__ void __launch_bounds__(192, 1)
           } else {
             const int r = ti.row0 + kc;
 #pragma unroll
+            for (int mh = 1; mh < C::MT; ++mh)
+#pragma unroll
+              for (int c = 0; c < 128 / C::CH; ++c)
+                tma_load_2d(sA + mh * C::A_PART + c * C::CHUNK_BYTES, &maps.a, fb,
+                            ti.m0 + mh * 128 + c * C::CH, r);
+#pragma unroll
             for (int c = 0; c < 128 / C::CH; ++c) {
               tma_load_2d(sA + c * C::CHUNK_BYTES, &maps.a, fb, ti.m0 + c * C::CH, r);
               if constexpr (C::SPLIT_A)
@@ -356,7 +370,7 @@ __global__ void __launch_bounds__(192, 1)
     uint32_t acc_phase = 0;
     bool ok = true;
     for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-      const TileInfo ti = decode_tile<C::BN_OUT, C::kWgrad>(args, t, C::BK);
+      const TileInfo ti = decode_tile<C::BN_OUT, C::kWgrad, C::MT>(args, t, C::BK);
       int good = 1;
       if (lane == 0) good = mbar_wait(tempty_bar + 8 * acc, acc_phase ^ 1u, tmo);
       good = __shfl_sync(0xffffffffu, good, 0);
@@ -366,7 +380,7 @@ __global__ void __launch_bounds__(192, 1)
         break;
       }
       tc_fence_after();
-      const uint32_t d_tmem = tmem_base + acc * BN;
+      const uint32_t d_tmem = tmem_base + acc * C::ACC_COLS;
       for (int kb = 0; kb < ti.nkb; ++kb) {
         if (lane == 0) good = mbar_wait(full_bar + 8 * stage, phase, tmo);
         good = __shfl_sync(0xffffffffu, good, 0);
@@ -402,6 +416,15 @@ __global__ void __launch_bounds__(192, 1)
             if constexpr (C::SPLIT_B)
               tc_mma<C::kTf32>(d_tmem, adesc, smem_desc_sw128(sB + C::B_PART + boff, blbo, 1024),
                                C::IDESC, 1u);
+#pragma unroll
+            for (int mh = 1; mh < C::MT; ++mh) {
+              // second m-tile: its own A rows, the same B tile
+              const uint64_t adesc2 = smem_desc_sw128(sA + mh * C::A_PART + aoff, albo, 1024);
+              tc_mma<C::kTf32>(d_tmem + mh * BN, adesc2, bdesc, C::IDESC, accum);
+              if constexpr (C::SPLIT_B)
+                tc_mma<C::kTf32>(d_tmem + mh * BN, adesc2,
+                                 smem_desc_sw128(sB + C::B_PART + boff, blbo, 1024), C::IDESC, 1u);
+            }
           }
           tc_commit(empty_bar + 8 * stage);
         }
@@ -436,12 +459,13 @@ __global__ void __launch_bounds__(192, 1)
   } else {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;                 // TMEM lane quarter = tile rows q*32..q*32+31
-    uint8_t* my_epi = epi_g + (warp - 2) * C::EPI_WARP_BYTES;
+    uint8_t* my_epi = epi_g + (warp - 2) * (C::EPI_WARP_BYTES + C::H1_WARP_BYTES);
+    uint8_t* my_h1 = my_epi + C::EPI_WARP_BYTES;
     int acc = 0;
     uint32_t acc_phase = 0;
 
     for (int t = blockIdx.x; t < total; t += gridDim.x) {
-      const TileInfo ti = decode_tile<C::BN_OUT, C::kWgrad>(args, t, C::BK);
+      const TileInfo ti = decode_tile<C::BN_OUT, C::kWgrad, C::MT>(args, t, C::BK);
       int good = 1;
       if (lane == 0) good = mbar_wait(tfull_bar + 8 * acc, acc_phase, tmo);
       good = __shfl_sync(0xffffffffu, good, 0);
@@ -450,21 +474,23 @@ __global__ void __launch_bounds__(192, 1)
         break;
       }
       tc_fence_after();
-      const uint32_t tacc = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
+      const uint32_t tacc = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * C::ACC_COLS;
       const int row = ti.row0 + q * 32 + lane;   // row-grouped modes: padded row of this thread
       const int orow = ti.row0 + q * 32;         // first row of this warp's output tiles
       float v[32];
 
       if constexpr (C::kWgrad) {
 #pragma unroll 1
-        for (int c = 0; c < BN / 32; ++c) {
+        for (int mc = 0; mc < C::MT * (BN / 32); ++mc) {
+          const int mh = mc / (BN / 32), c = mc % (BN / 32);
           if (ti.nkb > 0) {
-            tmem_ld32(tacc + c * 32, v);
+            tmem_ld32(tacc + mh * BN + c * 32, v);
           } else {
 #pragma unroll
             for (int i = 0; i < 32; ++i) v[i] = 0.f;
           }
-          store_tile<float>(args.out[0], ti.e, ti.m0 + q * 32, ti.n0 + c * 32, v, my_epi, lane);
+          store_tile<float>(args.out[0], ti.e, ti.m0 + mh * 128 + q * 32, ti.n0 + c * 32, v,
+                            my_epi, lane);
         }
       } else {
         // routing weight and liveness of this thread's row
@@ -510,31 +536,37 @@ __global__ void __launch_bounds__(192, 1)
             store_tile<float>(args.out[0], 0, orow, ti.n0 + c * 32, v, my_epi, lane);
           }
         } else {  // kDgradDown
-          // saved fp32 pre-activations of this row: gate at [0, I), up at [I, 2I)
+          // saved fp32 pre-activations of this row: gate at [0, I), up at [I, 2I);
+          // each lane copies its own row's 32 gate + 32 up values of a column
+          // chunk into shared memory with cp.async, one chunk ahead
           const float* h1row = static_cast<const float*>(args.h1) + static_cast<int64_t>(row) * 2 * args.I;
+          const float* h1s = reinterpret_cast<const float*>(my_h1) + lane * 68;
+          const uint32_t h1s_s = smem_u32(my_h1) + lane * 68 * 4;
+          auto prefetch = [&](int c) {
+            const int i0 = ti.n0 + c * 32;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              const int col = i0 + 4 * j;
+              const bool in = col < args.I;   // I % 8 == 0: 16-byte units are all in or all out
+              cp_async16(h1s_s + j * 16, in ? h1row + col : h1row, in ? 16u : 0u);
+              cp_async16(h1s_s + 128 + j * 16, in ? h1row + args.I + col : h1row, in ? 16u : 0u);
+            }
+            cp_async_commit();
+          };
+          prefetch(0);
           float dot = 0.f;
 #pragma unroll 1
           for (int c = 0; c < BN / 32; ++c) {
             tmem_ld32(tacc + c * 32, v);   // dA' (before the routing weight)
             const int i0 = ti.n0 + c * 32;
             float g[32], u[32];
-            if (i0 + 32 <= args.I) {
-              const float4* gp = reinterpret_cast<const float4*>(h1row + i0);
-              const float4* up = reinterpret_cast<const float4*>(h1row + args.I + i0);
+            cp_async_wait_all();
 #pragma unroll
-              for (int j = 0; j < 8; ++j) {
-                const float4 gv = __ldg(gp + j);
-                const float4 uv = __ldg(up + j);
-                g[4 * j] = gv.x; g[4 * j + 1] = gv.y; g[4 * j + 2] = gv.z; g[4 * j + 3] = gv.w;
-                u[4 * j] = uv.x; u[4 * j + 1] = uv.y; u[4 * j + 2] = uv.z; u[4 * j + 3] = uv.w;
-              }
-            } else {
-#pragma unroll
-              for (int i = 0; i < 32; ++i) {
-                const bool in = (i0 + i) < args.I;
-                g[i] = in ? __ldg(h1row + i0 + i) : 0.f;
-                u[i] = in ? __ldg(h1row + args.I + i0 + i) : 0.f;
-              }
+            for (int j = 0; j < 8; ++j) {
+              const float4 gv = *reinterpret_cast<const float4*>(h1s + 4 * j);
+              const float4 uv = *reinterpret_cast<const float4*>(h1s + 32 + 4 * j);
+              g[4 * j] = gv.x; g[4 * j + 1] = gv.y; g[4 * j + 2] = gv.z; g[4 * j + 3] = gv.w;
+              u[4 * j] = uv.x; u[4 * j + 1] = uv.y; u[4 * j + 2] = uv.z; u[4 * j + 3] = uv.w;
             }
             float dg[32], du[32], aw[32];
 #pragma unroll
@@ -547,6 +579,9 @@ __global__ void __launch_bounds__(192, 1)
               du[i] = da * pu;
               aw[i] = wrow * a;
             }
+            // every value of the staged row is consumed above: refill the
+            // buffer with the next chunk while this one is stored
+            if (c + 1 < BN / 32) prefetch(c + 1);
             if constexpr (C::kTf32) {
               // operands of the TF32 dgrad / wgrad products
 #pragma unroll

@@ -9,7 +9,7 @@ cudaError_t launch_gemm_bf16_wgrad(int mode, const GemmMaps& maps, const GemmArg
   using T = __nv_bfloat16;
   switch (mode) {
     case kWgradDown: return launch_gemm_t<T, kWgradDown, 256, 3>(maps, a, sms, st);
-    case kWgradGateUp: return launch_gemm_t<T, kWgradGateUp, 128, 4>(maps, a, sms, st);
+    case kWgradGateUp: return launch_gemm_t<T, kWgradGateUp, 128, 3>(maps, a, sms, st);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -98,5 +98,6 @@ cudaError_t launch_gemm(int mode, int elem_bytes, const GemmMaps& maps, const Ge
                         int num_sms, cudaStream_t st);
 // Column tile width (N) of the output for a mode, as used by launch_gemm.
 int gemm_block_n(int mode, int elem_bytes);
+int gemm_block_m(int mode, int elem_bytes);
 
 }  // namespace moe
