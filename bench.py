@@ -126,6 +126,24 @@ def committed_traffic(kernel):
         return None
 
 
+# ---------------------------------------------------------------- ranks
+
+
+def max_over_ranks(v, world, dist=None, device="cpu"):
+    """Largest value of v over all ranks (the slowest rank sets the time)."""
+    if world == 1 or dist is None:
+        return float(v)
+    import torch
+    t = torch.tensor([float(v)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(flops_per_step, world, ms_per_step):
+    """Whole-job TFLOP/s: every rank runs its own replica of the step."""
+    return world * flops_per_step / (ms_per_step * 1e-3) / 1e12
+
+
 # ---------------------------------------------------------------- clocks
 
 
@@ -297,12 +315,8 @@ def main():
         if world > 1:
             dist.barrier()
 
-    def max_over_ranks(v):
-        if world == 1:
-            return v
-        t = torch.tensor([v], dtype=torch.float64, device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
+    def ranks_max(v):
+        return max_over_ranks(v, world, dist if world > 1 else None, "cuda")
 
     clocks = ClockSampler(local)
     clocks.start()
@@ -321,7 +335,7 @@ def main():
     barrier()
     launches = moe_kernel_launch_count() - n0
     clocks.stop()
-    ms = max_over_ranks(ev0.elapsed_time(ev1)) / args.steps
+    ms = ranks_max(ev0.elapsed_time(ev1)) / args.steps
     run.check()
 
     # ---- per-kernel times (separate pass, library event timer on the same stream)
@@ -376,7 +390,7 @@ def main():
     torch.cuda.synchronize()
     n_e2e = max(3, min(args.steps, 50))
     barrier()
-    e2e_ms = max_over_ranks(timed(e2e_step, n_e2e))
+    e2e_ms = ranks_max(timed(e2e_step, n_e2e))
     run.check()
 
     # ---- accounting
@@ -387,7 +401,7 @@ def main():
     P = peaks["bf16_tflops_sustained"] * 1e12
     BW = peaks["hbm_gbs"] * 1e9
     step_flops = f_fwd + f_bwd
-    value = world * step_flops / (ms * 1e-3) / 1e12
+    value = job_throughput(step_flops, world, ms)
 
     # dominant kernel and its roofline
     work = kernel_work(r, e_active)
@@ -448,7 +462,7 @@ def main():
         "layer": {"fwd": layer_part(fwd_ms, f_fwd, b_fwd), "bwd": layer_part(bwd_ms, f_bwd, b_bwd)},
         "roofline": roofline,
         "kernels": per_kernel,
-        "e2e": {"value": round(world * step_flops / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+        "e2e": {"value": round(job_throughput(step_flops, world, e2e_ms), 2), "unit": "TFLOP/s",
                 "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": int(launches),
