@@ -47,10 +47,16 @@ int gemm_block_n(int mode, int elem_bytes) {
   return 256;
 }
 
-// Output rows per weight-gradient tile (two 128-row m-tiles for the bf16
-// gate_up weight gradient).
+// Output rows per weight-gradient m-tile (two 128-row tiles per CTA for the
+// bf16 gate_up weight gradient).
 int gemm_block_m(int mode, int elem_bytes) {
   return (mode == kWgradGateUp && elem_bytes == 2) ? 256 : 128;
+}
+
+// Rows of the K-major weight box of a dgrad: the bf16 gate_up dgrad runs as
+// CTA pairs, each holding half of the 256 columns.
+uint32_t dgrad_b_rows(int mode, int elem_bytes) {
+  return (mode == kDgradGateUp && elem_bytes == 2) ? 128 : 256;
 }
 
 }  // namespace moe
@@ -253,7 +259,7 @@ Layout layout(const moe_shape* s, int which) {
     return o;
   };
   L.err = take(256);
-  L.poff = take(sizeof(int) * (s->E + 1));
+  L.poff = take(sizeof(int) * 2 * (s->E + 1));   // padded offsets, then tile-pair prefix
   if (which == 0 || which == 1) L.blkhist = take(sizeof(int) * plan_blkhist_ints(Tk, s->E));
   if (which == 1) {
     L.counts = take(sizeof(int) * s->E);
@@ -472,7 +478,8 @@ moe_status moe_ffn_fwd(const moe_shape* s, const void* x, const int32_t* topk_id
 
   // gate_up GEMM + activation (+ fp32 pre-activations saved for the backward)
   GemmMaps m1;
-  bool ok = map2d(&m1.a, es, xp, H, R, H, BK, 128, SW);
+  const uint32_t AROWS = 128;
+  bool ok = map2d(&m1.a, es, xp, H, R, H, BK, AROWS, SW);
   if (es == 2) {
     ok = ok && map3d(&m1.b0, es, wgu, I, H, E, 2ll * I, 2ll * I * H, CH, BK, SW) &&
          map3d(&m1.b1, es, wgu + static_cast<size_t>(I) * es, I, H, E, 2ll * I, 2ll * I * H, CH,
@@ -503,7 +510,7 @@ moe_status moe_ffn_fwd(const moe_shape* s, const void* x, const int32_t* topk_id
   // down GEMM * routing weight -> fp32 rows Ow
   float* ow = at<float>(ws, L.ow);
   GemmMaps m2;
-  ok = map2d(&m2.a, es, aact, I, R, I, BK, 128, SW);
+  ok = map2d(&m2.a, es, aact, I, R, I, BK, AROWS, SW);
   if (es == 2) {
     ok = ok && map3d(&m2.b0, es, w_down, H, I, E, H, static_cast<int64_t>(H) * I, CH, BK, SW);
   } else {
@@ -612,8 +619,10 @@ moe_status moe_ffn_bwd(const moe_shape* s, const void* dy, const void* x, const 
 
   // (1) down dgrad + activation backward -> dH1 (gate | up), w*a, dw partials
   GemmMaps m1;
-  ok = map2d(&m1.a, es, dyp, H, R, H, BK, 128, SW) &&
-       map3d(&m1.b0, es, wd_op, H, I, E, H, static_cast<int64_t>(H) * I, BK, 256, SW);
+  const uint32_t AROWS = 128;
+  ok = map2d(&m1.a, es, dyp, H, R, H, BK, AROWS, SW) &&
+       map3d(&m1.b0, es, wd_op, H, I, E, H, static_cast<int64_t>(H) * I, BK,
+             dgrad_b_rows(kDgradDown, es), SW);
   if (!ok) return MOE_ERR_CUDA;
   m1.a2 = m1.a;
   m1.b1 = m1.b0;
@@ -664,8 +673,9 @@ moe_status moe_ffn_bwd(const moe_shape* s, const void* dy, const void* x, const 
   // (3) gate_up dgrad: dXp = dH1 Wgu[e]^T  (fp32 rows for the combine)
   float* dxp = at<float>(ws, L.dxp);
   GemmMaps m3;
-  ok = map2d(&m3.a, es, dh1, 2ll * I, R, 2ll * I, BK, 128, SW) &&
-       map3d(&m3.b0, es, wgu_op, 2ll * I, H, E, 2ll * I, 2ll * I * H, BK, 256, SW);
+  ok = map2d(&m3.a, es, dh1, 2ll * I, R, 2ll * I, BK, AROWS, SW) &&
+       map3d(&m3.b0, es, wgu_op, 2ll * I, H, E, 2ll * I, 2ll * I * H, BK,
+             dgrad_b_rows(kDgradGateUp, es), SW);
   if (!ok) return MOE_ERR_CUDA;
   m3.a2 = m3.a;
   m3.b1 = m3.b0;

@@ -2,17 +2,30 @@
 // multi-stage shared-memory ring, tcgen05.mma issued by one thread with the
 // fp32 accumulator in tensor memory (double-buffered), and a 4-warp epilogue
 // that reads the accumulator with tcgen05.ld, applies the mode's fused
-// elementwise work and writes 32x32 output tiles with TMA stores.
+// elementwise work and stores 32x32 tiles with coalesced global stores.
 //
-// One persistent CTA per SM walks a static tile sequence (CTA b takes tiles
-// b, b + grid, ...).  Warp roles: warp 0 = TMA producer, warp 1 = MMA issuer
-// (and tensor-memory owner), warps 2..5 = epilogue (warp w reads TMEM lanes
-// 32*(w%4) .. 32*(w%4)+31, i.e. tile rows).
+// bf16 kernels use the 2-SM form of the tensor-core MMA (cta_group::2): a
+// cluster of two CTAs computes a 256 x N tile.  Each CTA loads its own 128
+// rows of A and half (N/2 columns) of B into its shared memory; one thread
+// of the even CTA (the leader) issues M=256 MMAs that read both CTAs'
+// tiles, and each CTA's tensor memory receives the accumulator rows of its
+// own A rows.  A CTA therefore receives 2/3 of the operand bytes per FLOP
+// of a single-CTA 128 x N tile: the loads of a k-block (A 16 KB + B 16 KB
+// for N=256) then take less time than its MMAs, which a CTA's TMA delivery
+// rate otherwise cannot match.  fp32 storage (TF32
+// products) uses independent CTAs and the 1-SM form.
+//
+// Warp roles: warp 0 = TMA producer, warp 1 = MMA issuer (in the leader)
+// and tensor-memory owner, warps 2..5 = epilogue (warp w reads TMEM lanes
+// 32*(w%4) .. 32*(w%4)+31, i.e. tile rows).  Persistent: each CTA pair walks
+// a static sequence of work units.
 //
 // Row-grouped modes (forward and dgrad) tile the tile-padded expert-grouped
 // row space: expert e owns rows [poff[e], poff[e+1]), a multiple of 128, so
-// no M tile straddles two experts.  Tiles are ordered (expert, n, m) so the
-// CTAs running at the same time share one expert's weight columns in L2.
+// no M tile straddles two experts; a CTA pair takes two consecutive m-tiles
+// of one expert (the second CTA idles in its epilogue when the expert has an
+// odd number of m-tiles).  Units are ordered (expert, n, m-pair) so the
+// pairs running at the same time share one expert's weight columns in L2.
 // Weight-gradient modes tile the [E, M, N] output and contract over the
 // expert's padded rows (zero-filled padding contributes nothing).
 //
@@ -37,12 +50,18 @@ template <typename T, int MODE, int BN, int STAGES>
 struct GemmCfg {
   static constexpr int kES = sizeof(T);
   static constexpr bool kTf32 = (kES == 4);
-  static constexpr int BM = 128;
   static constexpr int BK = 128 / kES;           // elements in one 128-byte row
   static constexpr int CH = 128 / kES;           // MN-major chunk width (elements)
   static constexpr int MMA_K = 32 / kES;         // K of one tcgen05.mma
   static constexpr int KSTEPS = BK / MMA_K;      // MMAs per k-block (4)
   static constexpr bool kWgrad = (MODE == kWgradDown || MODE == kWgradGateUp);
+  // 2-SM MMA over a CTA pair for the bf16 forward GEMMs and the gate_up
+  // dgrad; the modes whose epilogue outweighs their MMAs (down dgrad, weight
+  // gradients) keep independent CTAs, as does TF32, since a pair's next MMA
+  // waits for both CTAs' epilogues
+  static constexpr bool CTA2 =
+      !kTf32 && (MODE == kFwdGateUp || MODE == kFwdDown || MODE == kDgradGateUp);
+  static constexpr int PAIR = CTA2 ? 2 : 1;
   // TF32 operands must be K-major (the fp32 path transposes the others into
   // the workspace first); 16-bit operands may be MN-major.
   static constexpr bool A_MN = kWgrad && !kTf32;
@@ -52,14 +71,15 @@ struct GemmCfg {
   // accumulator (about 16 bits of mantissa instead of 8).
   static constexpr bool SPLIT_A = (MODE == kWgradDown) && !kTf32;
   static constexpr bool SPLIT_B = (MODE == kWgradGateUp) && !kTf32;
-  // m-tiles of 128 rows per CTA tile: the gate_up weight gradient computes
-  // two, so its (split, hence doubled) B tile is loaded once for both.
+  // m-tiles of 128 rows per CTA tile: the bf16 gate_up weight gradient
+  // computes two, so its (split, hence doubled) B tile is loaded once for both
   static constexpr int MT = (MODE == kWgradGateUp && !kTf32) ? 2 : 1;
-  static constexpr int A_PART = BM * 128;
-  static constexpr int B_PART = BN * 128;
+  static constexpr int BN_CTA = BN / PAIR;       // B columns held by one CTA
+  static constexpr int A_PART = 128 * 128;       // 128 rows of A, one 128-byte K row each
+  static constexpr int B_PART = BN_CTA * 128;
   static constexpr int A_BYTES = A_PART * MT * (SPLIT_A ? 2 : 1);
   static constexpr int B_BYTES = B_PART * (SPLIT_B ? 2 : 1);
-  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;   // per CTA
   static constexpr int CHUNK_BYTES = BK * 128;   // one MN-major box
   // per epilogue warp: one 32x32 transpose tile, rows padded to 36 words;
   // the down dgrad also stages the saved pre-activations of its 32 rows
@@ -69,45 +89,54 @@ struct GemmCfg {
   static constexpr int EPI_BYTES = 4 * (EPI_WARP_BYTES + H1_WARP_BYTES);
   static constexpr int BAR_BYTES = (2 * STAGES + 5) * 8 + 16;
   static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + EPI_BYTES + BAR_BYTES;
-  static constexpr int ACC_COLS = MT * BN;   // TMEM columns of one tile's accumulator(s)
+  static constexpr int ACC_COLS = MT * BN;       // TMEM columns of one tile's accumulator(s)
   static constexpr int TMEM_COLS = (2 * ACC_COLS <= 256) ? 256 : 512;
-  static_assert(2 * ACC_COLS <= 512, "two accumulators must fit in tensor memory");
   // output columns produced per tile (gate_up: BN/2 gate + BN/2 up -> BN/2)
   static constexpr int BN_OUT = (MODE == kFwdGateUp) ? BN / 2 : BN;
-  static constexpr uint32_t IDESC = make_idesc(kTf32, A_MN, B_MN, BM, BN);
+  static constexpr uint32_t IDESC = make_idesc(kTf32, A_MN, B_MN, 128 * PAIR, BN);
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
-  static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "BN");
-  static_assert(!B_MN || BN % CH == 0, "MN-major B needs whole chunks");
+  static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "BN");
+  static_assert(2 * ACC_COLS <= 512, "two accumulators must fit in tensor memory");
+  static_assert(!B_MN || BN_CTA % CH == 0, "MN-major B needs whole chunks");
 };
 
 struct TileInfo {
   int e;       // expert
-  int row0;    // row-grouped: first padded row; wgrad: first padded row of expert
+  int row0;    // row-grouped: first padded row of this CTA; wgrad: first padded row of the expert
   int n0;      // first output column
-  int m0;      // wgrad: first output row
+  int m0;      // wgrad: first output row of this CTA
   int nkb;     // k-blocks
   int nt;      // column-tile index
+  bool active; // false when this CTA's 128 rows lie past the expert (or the output)
 };
 
-template <int BN_OUT, bool kWgrad, int MT = 1>
-__device__ __forceinline__ TileInfo decode_tile(const GemmArgs& a, int t, int bk) {
+// Work unit t of the schedule.  A unit is PAIR consecutive m-tiles with one
+// column tile; CTA `rank` of the pair takes m-tile unit_m*PAIR+rank (of
+// 128*MT output rows for the weight gradients).
+template <int BN_OUT, bool kWgrad, int PAIR, int MT = 1>
+__device__ __forceinline__ TileInfo decode_tile(const GemmArgs& a, int t, int bk, int rank) {
   TileInfo ti;
+  const int NT = a.n_tiles;
   if constexpr (kWgrad) {
-    const int per_e = a.m_tiles * a.n_tiles;
+    const int MP = (a.m_tiles + PAIR - 1) / PAIR;
+    const int per_e = MP * NT;
     ti.e = t / per_e;
     const int r = t - ti.e * per_e;
-    const int m = r / a.n_tiles;
-    ti.nt = r - m * a.n_tiles;
+    const int mp = r / NT;
+    ti.nt = r - mp * NT;
+    const int m = mp * PAIR + rank;
     ti.m0 = m * 128 * MT;
-    ti.n0 = ti.nt * BN_OUT;
+    ti.active = m < a.m_tiles;
     ti.row0 = __ldg(a.poff + ti.e);
     ti.nkb = (__ldg(a.poff + ti.e + 1) - ti.row0) / bk;
   } else {
-    const int NT = a.n_tiles;
+    // unit prefix of expert e: its tile pairs (PAIR = 2) or tiles (PAIR = 1)
+    const int* up = (PAIR == 2) ? a.poff + a.E + 1 : a.poff;
+    const int sh = (PAIR == 2) ? 0 : 7;
     int lo = 0, hi = a.E - 1;
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;
-      if ((__ldg(a.poff + mid) >> 7) * NT <= t)
+      if ((__ldg(up + mid) >> sh) * NT <= t)
         lo = mid;
       else
         hi = mid - 1;
@@ -115,15 +144,16 @@ __device__ __forceinline__ TileInfo decode_tile(const GemmArgs& a, int t, int bk
     ti.e = lo;
     const int p0 = __ldg(a.poff + lo);
     const int mt = (__ldg(a.poff + lo + 1) - p0) >> 7;
-    const int local = t - (p0 >> 7) * NT;
-    const int n = local / mt;
-    const int m = local - n * mt;
-    ti.nt = n;
+    const int mu = ((__ldg(up + lo + 1) - __ldg(up + lo)) >> sh);   // units of m
+    const int local = t - (__ldg(up + lo) >> sh) * NT;
+    ti.nt = local / mu;
+    const int m = (local - ti.nt * mu) * PAIR + rank;
+    ti.active = m < mt;
     ti.row0 = p0 + m * 128;
-    ti.n0 = n * BN_OUT;
     ti.m0 = 0;
     ti.nkb = a.num_kb;
   }
+  ti.n0 = ti.nt * BN_OUT;
   return ti;
 }
 
@@ -230,13 +260,17 @@ __global__ void __launch_bounds__(192, 1)
   const uint32_t empty_bar = bars + 8 * STAGES;      // [STAGES]
   const uint32_t tfull_bar = bars + 16 * STAGES;     // [2]
   const uint32_t tempty_bar = tfull_bar + 16;        // [2]
-  const uint32_t drain_bar = tempty_bar + 16;        // [1] error path only
+  const uint32_t drain_bar = tempty_bar + 16;        // [1] end of the MMA stream
   const uint32_t tmem_slot = drain_bar + 8;
   volatile uint32_t* tmem_slot_g =
       reinterpret_cast<volatile uint32_t*>(gbase + (tmem_slot - sbase));
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  // rank in the CTA pair; the even CTA issues the MMAs of both
+  const int crank = C::CTA2 ? static_cast<int>(cluster_ctarank()) : 0;
+  const bool leader = (crank == 0);
+  constexpr uint16_t kPairMask = 0x3;
 
   if (warp == 0 && lane == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -245,7 +279,7 @@ __global__ void __launch_bounds__(192, 1)
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(tfull_bar + 8 * s, 1);
-      mbar_init(tempty_bar + 8 * s, 128);
+      mbar_init(tempty_bar + 8 * s, 128 * C::PAIR);   // every epilogue thread of the pair
     }
     mbar_init(drain_bar, 1);
     fence_barrier_init();
@@ -253,22 +287,39 @@ __global__ void __launch_bounds__(192, 1)
     prefetch_tmap(&maps.b0);
   }
   if (warp == 1) {
-    tmem_alloc(tmem_slot, C::TMEM_COLS);
-    tmem_relinquish();
+    if constexpr (C::CTA2) {
+      tmem_alloc2(tmem_slot, C::TMEM_COLS);
+      tmem_relinquish2();
+    } else {
+      tmem_alloc(tmem_slot, C::TMEM_COLS);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
   __syncthreads();
+  if constexpr (C::CTA2) cluster_sync();   // both CTAs' barriers exist before any remote use
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot_g;
 
-  int total;
-  if constexpr (C::kWgrad)
-    total = args.E * args.m_tiles * args.n_tiles;
-  else
-    total = static_cast<int>(min(static_cast<int64_t>(__ldg(args.poff + args.E)), args.rows_max) >>
-                             7) *
-            args.n_tiles;
+  // The leader's barriers receive the TMA completions of both CTAs and the
+  // accumulator releases of both epilogues.
+  auto leader_addr = [&](uint32_t a) -> uint32_t { return C::CTA2 ? mapa_shared(a, 0) : a; };
 
+  int total;
+  if constexpr (C::kWgrad) {
+    total = args.E * ((args.m_tiles + C::PAIR - 1) / C::PAIR) * args.n_tiles;
+  } else {
+    // never past the workspace bound, even for an inconsistent caller plan
+    const int rows = static_cast<int>(
+        min(static_cast<int64_t>(__ldg(args.poff + args.E)), args.rows_max));
+    const int units = (C::PAIR == 2) ? (rows == __ldg(args.poff + args.E)
+                                            ? __ldg(args.poff + 2 * args.E + 1)
+                                            : 0)
+                                     : (rows >> 7);
+    total = units * args.n_tiles;
+  }
+  const int unit0 = blockIdx.x / C::PAIR;
+  const int ustride = gridDim.x / C::PAIR;
   const uint64_t tmo = args.timeout_ns;
 
   if (warp == 0) {
@@ -277,8 +328,8 @@ __global__ void __launch_bounds__(192, 1)
     uint32_t phase = 0;
     int64_t issued = 0;
     bool ok = true;
-    for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-      const TileInfo ti = decode_tile<C::BN_OUT, C::kWgrad, C::MT>(args, t, C::BK);
+    for (int t = unit0; t < total && ok; t += ustride) {
+      const TileInfo ti = decode_tile<C::BN_OUT, C::kWgrad, C::PAIR, C::MT>(args, t, C::BK, crank);
       for (int kb = 0; kb < ti.nkb; ++kb) {
         int good = 1;
         if (lane == 0) good = mbar_wait(empty_bar + 8 * stage, phase ^ 1u, tmo);
@@ -290,59 +341,69 @@ __global__ void __launch_bounds__(192, 1)
         }
         if (lane == 0) {
           const uint32_t fb = full_bar + 8 * stage;
+          const uint32_t fbt = leader_addr(fb);
           const uint32_t sA = s_stages + stage * C::STAGE_BYTES;
           const uint32_t sB = sA + C::A_BYTES;
-          mbar_arrive_expect_tx(fb, C::STAGE_BYTES);
+          // the leader expects the bytes of both CTAs of the pair
+          if (leader) mbar_arrive_expect_tx(fb, C::PAIR * C::STAGE_BYTES);
+          auto load2 = [&](uint32_t dst, const CUtensorMap* m, int c0, int c1) {
+            if constexpr (C::CTA2)
+              tma_load_2d_g2(dst, m, fbt, c0, c1);
+            else
+              tma_load_2d(dst, m, fbt, c0, c1);
+          };
+          auto load3 = [&](uint32_t dst, const CUtensorMap* m, int c0, int c1, int c2) {
+            if constexpr (C::CTA2)
+              tma_load_3d_g2(dst, m, fbt, c0, c1, c2);
+            else
+              tma_load_3d(dst, m, fbt, c0, c1, c2);
+          };
           const int kc = kb * C::BK;
-          if constexpr (MODE == kFwdGateUp && C::B_MN) {
-            tma_load_2d(sA, &maps.a, fb, kc, ti.row0);
-            constexpr int HALF_CH = (BN / 2) / C::CH;
+          // ---- A: this CTA's 128 rows
+          if constexpr (C::kWgrad && !C::A_MN) {
+            load2(sA, &maps.a, ti.row0 + kc, ti.m0);   // K-major (transposed) activations
+          } else if constexpr (!C::A_MN) {
+            load2(sA, &maps.a, kc, ti.row0);
+          } else {
+            // MN-major chunks (128 B of M x BK rows): per m-tile, hi then lo
+            // when split
+            constexpr int NPART = C::SPLIT_A ? 2 : 1;
 #pragma unroll
-            for (int c = 0; c < HALF_CH; ++c) {
-              tma_load_3d(sB + c * C::CHUNK_BYTES, &maps.b0, fb, ti.n0 + c * C::CH, kc, ti.e);
-              tma_load_3d(sB + (HALF_CH + c) * C::CHUNK_BYTES, &maps.b1, fb, ti.n0 + c * C::CH,
-                          kc, ti.e);
-            }
+            for (int mh = 0; mh < C::MT; ++mh)
+#pragma unroll
+              for (int part = 0; part < NPART; ++part)
+#pragma unroll
+                for (int c = 0; c < 128 / C::CH; ++c)
+                  load2(sA + (mh * NPART + part) * C::A_PART + c * C::CHUNK_BYTES,
+                        part ? &maps.a2 : &maps.a, ti.m0 + mh * 128 + c * C::CH, ti.row0 + kc);
+          }
+          // ---- B: this CTA's BN_CTA columns
+          const int nb = ti.n0 + crank * C::BN_CTA;
+          if constexpr (MODE == kFwdGateUp && C::B_MN) {
+            // the gate half from the even CTA, the up half from the odd one
+            const CUtensorMap* view = crank ? &maps.b1 : &maps.b0;
+#pragma unroll
+            for (int c = 0; c < C::BN_CTA / C::CH; ++c)
+              load3(sB + c * C::CHUNK_BYTES, view, ti.n0 + c * C::CH, kc, ti.e);
           } else if constexpr (MODE == kFwdGateUp) {
             // K-major (transposed) weights: gate rows then up rows of the tile
-            tma_load_2d(sA, &maps.a, fb, kc, ti.row0);
-            tma_load_3d(sB, &maps.b0, fb, kc, ti.n0, ti.e);
-            tma_load_3d(sB + (BN / 2) * 128, &maps.b1, fb, kc, ti.n0, ti.e);
+            load3(sB, &maps.b0, kc, ti.n0, ti.e);
+            load3(sB + (BN / 2) * 128, &maps.b1, kc, ti.n0, ti.e);
           } else if constexpr (MODE == kFwdDown && C::B_MN) {
-            tma_load_2d(sA, &maps.a, fb, kc, ti.row0);
 #pragma unroll
-            for (int c = 0; c < BN / C::CH; ++c)
-              tma_load_3d(sB + c * C::CHUNK_BYTES, &maps.b0, fb, ti.n0 + c * C::CH, kc, ti.e);
-          } else if constexpr (MODE == kFwdDown || MODE == kDgradDown || MODE == kDgradGateUp) {
-            tma_load_2d(sA, &maps.a, fb, kc, ti.row0);
-            tma_load_3d(sB, &maps.b0, fb, kc, ti.n0, ti.e);
-          } else if constexpr (!C::A_MN) {
-            // weight gradient from K-major (transposed) activations
-            const int r = ti.row0 + kc;
-            tma_load_2d(sA, &maps.a, fb, r, ti.m0);
-            tma_load_2d(sB, &maps.b0, fb, r, ti.n0);
+            for (int c = 0; c < C::BN_CTA / C::CH; ++c)
+              load3(sB + c * C::CHUNK_BYTES, &maps.b0, nb + c * C::CH, kc, ti.e);
+          } else if constexpr (!C::kWgrad) {
+            load3(sB, &maps.b0, kc, nb, ti.e);   // K-major weights, box {BK, BN_CTA}
+          } else if constexpr (!C::B_MN) {
+            load2(sB, &maps.b0, ti.row0 + kc, nb);
           } else {
-            const int r = ti.row0 + kc;
 #pragma unroll
-            for (int mh = 1; mh < C::MT; ++mh)
+            for (int part = 0; part < (C::SPLIT_B ? 2 : 1); ++part)
 #pragma unroll
-              for (int c = 0; c < 128 / C::CH; ++c)
-                tma_load_2d(sA + mh * C::A_PART + c * C::CHUNK_BYTES, &maps.a, fb,
-                            ti.m0 + mh * 128 + c * C::CH, r);
-#pragma unroll
-            for (int c = 0; c < 128 / C::CH; ++c) {
-              tma_load_2d(sA + c * C::CHUNK_BYTES, &maps.a, fb, ti.m0 + c * C::CH, r);
-              if constexpr (C::SPLIT_A)
-                tma_load_2d(sA + C::A_PART + c * C::CHUNK_BYTES, &maps.a2, fb, ti.m0 + c * C::CH,
-                            r);
-            }
-#pragma unroll
-            for (int c = 0; c < BN / C::CH; ++c) {
-              tma_load_2d(sB + c * C::CHUNK_BYTES, &maps.b0, fb, ti.n0 + c * C::CH, r);
-              if constexpr (C::SPLIT_B)
-                tma_load_2d(sB + C::B_PART + c * C::CHUNK_BYTES, &maps.b1, fb, ti.n0 + c * C::CH,
-                            r);
-            }
+              for (int c = 0; c < C::BN_CTA / C::CH; ++c)
+                load2(sB + part * C::B_PART + c * C::CHUNK_BYTES, part ? &maps.b1 : &maps.b0,
+                      nb + c * C::CH, ti.row0 + kc);
           }
         }
         __syncwarp();
@@ -353,8 +414,9 @@ __global__ void __launch_bounds__(192, 1)
         }
       }
     }
-    // Before the CTA may exit, every load issued must have landed.
-    if (lane == 0) {
+    // Before the CTAs may exit, every load issued must have landed: the
+    // leader's full barriers count the bytes of both CTAs.
+    if (lane == 0 && leader) {
       for (int s = 0; s < STAGES; ++s) {
         const int64_t n_s = (issued > s) ? (issued - 1 - s) / STAGES + 1 : 0;
         if (n_s > 0 &&
@@ -364,25 +426,16 @@ __global__ void __launch_bounds__(192, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    int stage = 0;
-    uint32_t phase = 0;
-    int acc = 0;
-    uint32_t acc_phase = 0;
-    bool ok = true;
-    for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-      const TileInfo ti = decode_tile<C::BN_OUT, C::kWgrad, C::MT>(args, t, C::BK);
-      int good = 1;
-      if (lane == 0) good = mbar_wait(tempty_bar + 8 * acc, acc_phase ^ 1u, tmo);
-      good = __shfl_sync(0xffffffffu, good, 0);
-      if (!good) {
-        if (lane == 0) record_error(args.err, kErrTimeout);
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      const uint32_t d_tmem = tmem_base + acc * C::ACC_COLS;
-      for (int kb = 0; kb < ti.nkb; ++kb) {
-        if (lane == 0) good = mbar_wait(full_bar + 8 * stage, phase, tmo);
+    if (leader) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      for (int t = unit0; t < total && ok; t += ustride) {
+        const TileInfo ti = decode_tile<C::BN_OUT, C::kWgrad, C::PAIR, C::MT>(args, t, C::BK, crank);
+        int good = 1;
+        if (lane == 0) good = mbar_wait(tempty_bar + 8 * acc, acc_phase ^ 1u, tmo);
         good = __shfl_sync(0xffffffffu, good, 0);
         if (!good) {
           if (lane == 0) record_error(args.err, kErrTimeout);
@@ -390,69 +443,88 @@ __global__ void __launch_bounds__(192, 1)
           break;
         }
         tc_fence_after();
-        if (lane == 0) {
-          const uint32_t sA = s_stages + stage * C::STAGE_BYTES;
-          const uint32_t sB = sA + C::A_BYTES;
-#pragma unroll
-          for (int kk = 0; kk < C::KSTEPS; ++kk) {
-            uint32_t aoff, boff;
-            if constexpr (C::A_MN)
-              aoff = kk * C::MMA_K * 128;
-            else
-              aoff = kk * 32;
-            if constexpr (C::B_MN)
-              boff = kk * C::MMA_K * 128;
-            else
-              boff = kk * 32;
-            const uint32_t albo = C::A_MN ? C::CHUNK_BYTES : 16;
-            const uint32_t blbo = C::B_MN ? C::CHUNK_BYTES : 16;
-            const uint64_t adesc = smem_desc_sw128(sA + aoff, albo, 1024);
-            const uint64_t bdesc = smem_desc_sw128(sB + boff, blbo, 1024);
-            const uint32_t accum = (kb | kk) != 0 ? 1u : 0u;
-            tc_mma<C::kTf32>(d_tmem, adesc, bdesc, C::IDESC, accum);
-            if constexpr (C::SPLIT_A)
-              tc_mma<C::kTf32>(d_tmem, smem_desc_sw128(sA + C::A_PART + aoff, albo, 1024), bdesc,
-                               C::IDESC, 1u);
-            if constexpr (C::SPLIT_B)
-              tc_mma<C::kTf32>(d_tmem, adesc, smem_desc_sw128(sB + C::B_PART + boff, blbo, 1024),
-                               C::IDESC, 1u);
-#pragma unroll
-            for (int mh = 1; mh < C::MT; ++mh) {
-              // second m-tile: its own A rows, the same B tile
-              const uint64_t adesc2 = smem_desc_sw128(sA + mh * C::A_PART + aoff, albo, 1024);
-              tc_mma<C::kTf32>(d_tmem + mh * BN, adesc2, bdesc, C::IDESC, accum);
-              if constexpr (C::SPLIT_B)
-                tc_mma<C::kTf32>(d_tmem + mh * BN, adesc2,
-                                 smem_desc_sw128(sB + C::B_PART + boff, blbo, 1024), C::IDESC, 1u);
-            }
+        const uint32_t d_tmem = tmem_base + acc * C::ACC_COLS;
+        for (int kb = 0; kb < ti.nkb; ++kb) {
+          if (lane == 0) good = mbar_wait(full_bar + 8 * stage, phase, tmo);
+          good = __shfl_sync(0xffffffffu, good, 0);
+          if (!good) {
+            if (lane == 0) record_error(args.err, kErrTimeout);
+            ok = false;
+            break;
           }
-          tc_commit(empty_bar + 8 * stage);
+          tc_fence_after();
+          if (lane == 0) {
+            const uint32_t sA = s_stages + stage * C::STAGE_BYTES;
+            const uint32_t sB = sA + C::A_BYTES;
+            auto mma = [&](uint64_t ad, uint64_t bd, uint32_t accum) {
+              if constexpr (C::CTA2)
+                tc_mma2(d_tmem, ad, bd, C::IDESC, accum);
+              else
+                tc_mma<C::kTf32>(d_tmem, ad, bd, C::IDESC, accum);
+            };
+#pragma unroll
+            for (int kk = 0; kk < C::KSTEPS; ++kk) {
+              const uint32_t aoff = C::A_MN ? kk * C::MMA_K * 128 : kk * 32;
+              const uint32_t boff = C::B_MN ? kk * C::MMA_K * 128 : kk * 32;
+              const uint32_t albo = C::A_MN ? C::CHUNK_BYTES : 16;
+              const uint32_t blbo = C::B_MN ? C::CHUNK_BYTES : 16;
+              const uint64_t adesc = smem_desc_sw128(sA + aoff, albo, 1024);
+              const uint64_t bdesc = smem_desc_sw128(sB + boff, blbo, 1024);
+              mma(adesc, bdesc, (kb | kk) != 0 ? 1u : 0u);
+              if constexpr (C::SPLIT_A)
+                mma(smem_desc_sw128(sA + C::A_PART + aoff, albo, 1024), bdesc, 1u);
+              if constexpr (C::SPLIT_B)
+                mma(adesc, smem_desc_sw128(sB + C::B_PART + boff, blbo, 1024), 1u);
+#pragma unroll
+              for (int mh = 1; mh < C::MT; ++mh) {
+                // further m-tiles (1-SM only): their own A rows, the same B
+                const uint64_t ad2 = smem_desc_sw128(sA + mh * C::A_PART + aoff, albo, 1024);
+                const uint32_t d2 = d_tmem + mh * BN;
+                tc_mma<C::kTf32>(d2, ad2, bdesc, C::IDESC, (kb | kk) != 0 ? 1u : 0u);
+                if constexpr (C::SPLIT_B)
+                  tc_mma<C::kTf32>(d2, ad2, smem_desc_sw128(sB + C::B_PART + boff, blbo, 1024),
+                                   C::IDESC, 1u);
+              }
+            }
+            // the stage is free in both CTAs once these MMAs have read it
+            if constexpr (C::CTA2)
+              tc_commit2_mc(empty_bar + 8 * stage, kPairMask);
+            else
+              tc_commit(empty_bar + 8 * stage);
+          }
+          __syncwarp();
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        if (lane == 0) {
+          if (ti.nkb > 0) {
+            if constexpr (C::CTA2)
+              tc_commit2_mc(tfull_bar + 8 * acc, kPairMask);
+            else
+              tc_commit(tfull_bar + 8 * acc);
+          } else {
+            // nothing to accumulate (an expert without rows): zeros are stored
+            mbar_arrive(tfull_bar + 8 * acc);
+            if constexpr (C::CTA2) mbar_arrive_cluster(mapa_shared(tfull_bar + 8 * acc, 1));
+          }
         }
         __syncwarp();
-        if (++stage == STAGES) {
-          stage = 0;
-          phase ^= 1u;
+        if (++acc == 2) {
+          acc = 0;
+          acc_phase ^= 1u;
         }
       }
-      if (!ok) break;
+      // End of the MMA stream (also after a timeout): one more commit
+      // arrives on the drain barrier of both CTAs once every MMA and every
+      // stage release issued before it has completed.
       if (lane == 0) {
-        if (ti.nkb > 0)
-          tc_commit(tfull_bar + 8 * acc);
+        if constexpr (C::CTA2)
+          tc_commit2_mc(drain_bar, kPairMask);
         else
-          mbar_arrive(tfull_bar + 8 * acc);
-      }
-      __syncwarp();
-      if (++acc == 2) {
-        acc = 0;
-        acc_phase ^= 1u;
-      }
-    }
-    if (!ok) {
-      // Unwinding after a timeout: let the MMAs already issued finish before
-      // tensor memory is released.
-      if (lane == 0) {
-        tc_commit(drain_bar);
-        if (!mbar_wait(drain_bar, 0, kDrainNs)) record_error(args.err, kErrTimeout);
+          tc_commit(drain_bar);
       }
       __syncwarp();
     }
@@ -464,8 +536,8 @@ __global__ void __launch_bounds__(192, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
 
-    for (int t = blockIdx.x; t < total; t += gridDim.x) {
-      const TileInfo ti = decode_tile<C::BN_OUT, C::kWgrad, C::MT>(args, t, C::BK);
+    for (int t = unit0; t < total; t += ustride) {
+      const TileInfo ti = decode_tile<C::BN_OUT, C::kWgrad, C::PAIR, C::MT>(args, t, C::BK, crank);
       int good = 1;
       if (lane == 0) good = mbar_wait(tfull_bar + 8 * acc, acc_phase, tmo);
       good = __shfl_sync(0xffffffffu, good, 0);
@@ -474,148 +546,159 @@ __global__ void __launch_bounds__(192, 1)
         break;
       }
       tc_fence_after();
-      const uint32_t tacc = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * C::ACC_COLS;
-      const int row = ti.row0 + q * 32 + lane;   // row-grouped modes: padded row of this thread
-      const int orow = ti.row0 + q * 32;         // first row of this warp's output tiles
-      float v[32];
+      if (ti.active) {
+        const uint32_t tacc = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * C::ACC_COLS;
+        const int row = ti.row0 + q * 32 + lane;   // row-grouped modes: padded row of this thread
+        const int orow = ti.row0 + q * 32;         // first row of this warp's output tiles
+        float v[32];
 
-      if constexpr (C::kWgrad) {
+        if constexpr (C::kWgrad) {
 #pragma unroll 1
-        for (int mc = 0; mc < C::MT * (BN / 32); ++mc) {
-          const int mh = mc / (BN / 32), c = mc % (BN / 32);
-          if (ti.nkb > 0) {
-            tmem_ld32(tacc + mh * BN + c * 32, v);
-          } else {
+          for (int mc = 0; mc < C::MT * (BN / 64); ++mc) {
+            const int mh = mc / (BN / 64), c = mc % (BN / 64);
+            float w2[64];
+            if (ti.nkb > 0) {
+              tmem_ld64(tacc + mh * BN + c * 64, w2);
+            } else {
 #pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] = 0.f;
+              for (int i = 0; i < 64; ++i) w2[i] = 0.f;
+            }
+            const int r0 = ti.m0 + mh * 128 + q * 32;
+            store_tile<float>(args.out[0], ti.e, r0, ti.n0 + c * 64,
+                              *reinterpret_cast<const float(*)[32]>(w2), my_epi, lane);
+            store_tile<float>(args.out[0], ti.e, r0, ti.n0 + c * 64 + 32,
+                              *reinterpret_cast<const float(*)[32]>(w2 + 32), my_epi, lane);
           }
-          store_tile<float>(args.out[0], ti.e, ti.m0 + mh * 128 + q * 32, ti.n0 + c * 32, v,
-                            my_epi, lane);
-        }
-      } else {
-        // routing weight and liveness of this thread's row
-        const int local = row - __ldg(args.poff + ti.e);
-        const bool live = local < __ldg(args.counts + ti.e);
-        float wrow = 0.f;
-        if constexpr (MODE == kFwdDown || MODE == kDgradDown) {
-          const int gi = __ldg(args.offsets + ti.e) + local;
-          if (live && gi < args.tk) {
-            const int slot = __ldg(args.perm + gi);
-            if (slot >= 0 && slot < args.tk) wrow = __ldg(args.topk_w + slot);
+        } else {
+          // routing weight and liveness of this thread's row
+          const int local = row - __ldg(args.poff + ti.e);
+          const bool live = local < __ldg(args.counts + ti.e);
+          float wrow = 0.f;
+          if constexpr (MODE == kFwdDown || MODE == kDgradDown) {
+            const int gi = __ldg(args.offsets + ti.e) + local;
+            if (live && gi < args.tk) {
+              const int slot = __ldg(args.perm + gi);
+              if (slot >= 0 && slot < args.tk) wrow = __ldg(args.topk_w + slot);
+            }
           }
-        }
-        if constexpr (MODE == kFwdGateUp) {
+          if constexpr (MODE == kFwdGateUp) {
 #pragma unroll 1
-          for (int c = 0; c < BN / 64; ++c) {
-            float u[32];
-            tmem_ld32(tacc + c * 32, v);
-            tmem_ld32(tacc + BN / 2 + c * 32, u);
-            if (args.save_h1) {
-              store_tile<float>(args.out[1], 0, orow, ti.n0 + c * 32, v, my_epi, lane);
-              store_tile<float>(args.out[2], 0, orow, ti.n0 + c * 32, u, my_epi, lane);
-            }
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              v[i] = act_fwd<T>(args.act, v[i], u[i], args.limit, args.alpha);
-              if constexpr (C::kTf32) v[i] = round_tf32(v[i]);   // operand of the down GEMM
-            }
-            store_tile<T>(args.out[0], 0, orow, ti.n0 + c * 32, v, my_epi, lane);
-          }
-        } else if constexpr (MODE == kFwdDown) {
-#pragma unroll 1
-          for (int c = 0; c < BN / 32; ++c) {
-            tmem_ld32(tacc + c * 32, v);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] *= wrow;
-            store_tile<float>(args.out[0], 0, orow, ti.n0 + c * 32, v, my_epi, lane);
-          }
-        } else if constexpr (MODE == kDgradGateUp) {
-#pragma unroll 1
-          for (int c = 0; c < BN / 32; ++c) {
-            tmem_ld32(tacc + c * 32, v);
-            store_tile<float>(args.out[0], 0, orow, ti.n0 + c * 32, v, my_epi, lane);
-          }
-        } else {  // kDgradDown
-          // saved fp32 pre-activations of this row: gate at [0, I), up at [I, 2I);
-          // each lane copies its own row's 32 gate + 32 up values of a column
-          // chunk into shared memory with cp.async, one chunk ahead
-          const float* h1row = static_cast<const float*>(args.h1) + static_cast<int64_t>(row) * 2 * args.I;
-          const float* h1s = reinterpret_cast<const float*>(my_h1) + lane * 68;
-          const uint32_t h1s_s = smem_u32(my_h1) + lane * 68 * 4;
-          auto prefetch = [&](int c) {
-            const int i0 = ti.n0 + c * 32;
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              const int col = i0 + 4 * j;
-              const bool in = col < args.I;   // I % 8 == 0: 16-byte units are all in or all out
-              cp_async16(h1s_s + j * 16, in ? h1row + col : h1row, in ? 16u : 0u);
-              cp_async16(h1s_s + 128 + j * 16, in ? h1row + args.I + col : h1row, in ? 16u : 0u);
-            }
-            cp_async_commit();
-          };
-          prefetch(0);
-          float dot = 0.f;
-#pragma unroll 1
-          for (int c = 0; c < BN / 32; ++c) {
-            tmem_ld32(tacc + c * 32, v);   // dA' (before the routing weight)
-            const int i0 = ti.n0 + c * 32;
-            float g[32], u[32];
-            cp_async_wait_all();
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              const float4 gv = *reinterpret_cast<const float4*>(h1s + 4 * j);
-              const float4 uv = *reinterpret_cast<const float4*>(h1s + 32 + 4 * j);
-              g[4 * j] = gv.x; g[4 * j + 1] = gv.y; g[4 * j + 2] = gv.z; g[4 * j + 3] = gv.w;
-              u[4 * j] = uv.x; u[4 * j + 1] = uv.y; u[4 * j + 2] = uv.z; u[4 * j + 3] = uv.w;
-            }
-            float dg[32], du[32], aw[32];
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              float a, pg, pu;
-              act_bwd(args.act, g[i], u[i], args.limit, args.alpha, a, pg, pu);
-              dot += v[i] * a;
-              const float da = wrow * v[i];
-              dg[i] = da * pg;
-              du[i] = da * pu;
-              aw[i] = wrow * a;
-            }
-            // every value of the staged row is consumed above: refill the
-            // buffer with the next chunk while this one is stored
-            if (c + 1 < BN / 32) prefetch(c + 1);
-            if constexpr (C::kTf32) {
-              // operands of the TF32 dgrad / wgrad products
+            for (int c = 0; c < BN / 64; ++c) {
+              float u[32];
+              tmem_ld32(tacc + c * 32, v);
+              tmem_ld32(tacc + BN / 2 + c * 32, u);
+              if (args.save_h1) {
+                store_tile<float>(args.out[1], 0, orow, ti.n0 + c * 32, v, my_epi, lane);
+                store_tile<float>(args.out[2], 0, orow, ti.n0 + c * 32, u, my_epi, lane);
+              }
 #pragma unroll
               for (int i = 0; i < 32; ++i) {
-                dg[i] = round_tf32(dg[i]);
-                du[i] = round_tf32(du[i]);
-                aw[i] = round_tf32(aw[i]);
+                v[i] = act_fwd<T>(args.act, v[i], u[i], args.limit, args.alpha);
+                if constexpr (C::kTf32) v[i] = round_tf32(v[i]);   // operand of the down GEMM
               }
-              store_tile<T>(args.out[0], 0, orow, i0, dg, my_epi, lane);
-              store_tile<T>(args.out[1], 0, orow, i0, du, my_epi, lane);
-              store_tile<T>(args.out[2], 0, orow, i0, aw, my_epi, lane);
-            } else {
-              // bf16 hi parts (operands of the dgrad and the wgrads) and lo
-              // parts (the remainders, operands of the wgrads only)
-              float lo[32];
-#pragma unroll
-              for (int i = 0; i < 32; ++i) split_bf16(dg[i], dg[i], lo[i]);
-              store_tile<T>(args.out[0], 0, orow, i0, dg, my_epi, lane);
-              store_tile<T>(args.out[3], 0, orow, i0, lo, my_epi, lane);
-#pragma unroll
-              for (int i = 0; i < 32; ++i) split_bf16(du[i], du[i], lo[i]);
-              store_tile<T>(args.out[1], 0, orow, i0, du, my_epi, lane);
-              store_tile<T>(args.out[4], 0, orow, i0, lo, my_epi, lane);
-#pragma unroll
-              for (int i = 0; i < 32; ++i) split_bf16(aw[i], aw[i], lo[i]);
-              store_tile<T>(args.out[2], 0, orow, i0, aw, my_epi, lane);
-              store_tile<T>(args.out[5], 0, orow, i0, lo, my_epi, lane);
+              store_tile<T>(args.out[0], 0, orow, ti.n0 + c * 32, v, my_epi, lane);
             }
+          } else if constexpr (MODE == kFwdDown || MODE == kDgradGateUp) {
+            // fp32 rows for the combine; the down projection also applies the
+            // routing weight of the row's slot
+            const float scale = (MODE == kFwdDown) ? wrow : 1.f;
+#pragma unroll 1
+            for (int c = 0; c < BN / 64; ++c) {
+              float w2[64];
+              tmem_ld64(tacc + c * 64, w2);
+#pragma unroll
+              for (int i = 0; i < 64; ++i) w2[i] *= scale;
+              store_tile<float>(args.out[0], 0, orow, ti.n0 + c * 64,
+                                *reinterpret_cast<const float(*)[32]>(w2), my_epi, lane);
+              store_tile<float>(args.out[0], 0, orow, ti.n0 + c * 64 + 32,
+                                *reinterpret_cast<const float(*)[32]>(w2 + 32), my_epi, lane);
+            }
+          } else {  // kDgradDown
+            // saved fp32 pre-activations of this row: gate at [0, I), up at [I, 2I);
+            // each lane copies its own row's 32 gate + 32 up values of a column
+            // chunk into shared memory with cp.async, one chunk ahead
+            const float* h1row = static_cast<const float*>(args.h1) + static_cast<int64_t>(row) * 2 * args.I;
+            const float* h1s = reinterpret_cast<const float*>(my_h1) + lane * 68;
+            const uint32_t h1s_s = smem_u32(my_h1) + lane * 68 * 4;
+            auto prefetch = [&](int c) {
+              const int i0 = ti.n0 + c * 32;
+#pragma unroll
+              for (int j = 0; j < 8; ++j) {
+                const int col = i0 + 4 * j;
+                const bool in = col < args.I;   // I % 8 == 0: 16-byte units are all in or all out
+                cp_async16(h1s_s + j * 16, in ? h1row + col : h1row, in ? 16u : 0u);
+                cp_async16(h1s_s + 128 + j * 16, in ? h1row + args.I + col : h1row, in ? 16u : 0u);
+              }
+              cp_async_commit();
+            };
+            prefetch(0);
+            float dot = 0.f;
+#pragma unroll 1
+            for (int c = 0; c < BN / 32; ++c) {
+              tmem_ld32(tacc + c * 32, v);   // dA' (before the routing weight)
+              const int i0 = ti.n0 + c * 32;
+              float g[32], u[32];
+              cp_async_wait_all();
+#pragma unroll
+              for (int j = 0; j < 8; ++j) {
+                const float4 gv = *reinterpret_cast<const float4*>(h1s + 4 * j);
+                const float4 uv = *reinterpret_cast<const float4*>(h1s + 32 + 4 * j);
+                g[4 * j] = gv.x; g[4 * j + 1] = gv.y; g[4 * j + 2] = gv.z; g[4 * j + 3] = gv.w;
+                u[4 * j] = uv.x; u[4 * j + 1] = uv.y; u[4 * j + 2] = uv.z; u[4 * j + 3] = uv.w;
+              }
+              float dg[32], du[32], aw[32];
+#pragma unroll
+              for (int i = 0; i < 32; ++i) {
+                float a, pg, pu;
+                act_bwd(args.act, g[i], u[i], args.limit, args.alpha, a, pg, pu);
+                dot += v[i] * a;
+                const float da = wrow * v[i];
+                dg[i] = da * pg;
+                du[i] = da * pu;
+                aw[i] = wrow * a;
+              }
+              // every value of the staged row is consumed above: refill the
+              // buffer with the next chunk while this one is stored
+              if (c + 1 < BN / 32) prefetch(c + 1);
+              if constexpr (C::kTf32) {
+                // operands of the TF32 dgrad / wgrad products
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                  dg[i] = round_tf32(dg[i]);
+                  du[i] = round_tf32(du[i]);
+                  aw[i] = round_tf32(aw[i]);
+                }
+                store_tile<T>(args.out[0], 0, orow, i0, dg, my_epi, lane);
+                store_tile<T>(args.out[1], 0, orow, i0, du, my_epi, lane);
+                store_tile<T>(args.out[2], 0, orow, i0, aw, my_epi, lane);
+              } else {
+                // bf16 hi parts (operands of the dgrad and the wgrads) and lo
+                // parts (the remainders, operands of the wgrads only)
+                float lo[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) split_bf16(dg[i], dg[i], lo[i]);
+                store_tile<T>(args.out[0], 0, orow, i0, dg, my_epi, lane);
+                store_tile<T>(args.out[3], 0, orow, i0, lo, my_epi, lane);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) split_bf16(du[i], du[i], lo[i]);
+                store_tile<T>(args.out[1], 0, orow, i0, du, my_epi, lane);
+                store_tile<T>(args.out[4], 0, orow, i0, lo, my_epi, lane);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) split_bf16(aw[i], aw[i], lo[i]);
+                store_tile<T>(args.out[2], 0, orow, i0, aw, my_epi, lane);
+                store_tile<T>(args.out[5], 0, orow, i0, lo, my_epi, lane);
+              }
+            }
+            args.dwpart[static_cast<int64_t>(ti.nt) * args.rows_max + row] = live ? dot : 0.f;
           }
-          args.dwpart[static_cast<int64_t>(ti.nt) * args.rows_max + row] = live ? dot : 0.f;
         }
       }
+      // release the accumulator to the MMA issuer (the leader)
       tc_fence_before();
-      mbar_arrive(tempty_bar + 8 * acc);
+      if constexpr (C::CTA2)
+        mbar_arrive_cluster(leader_addr(tempty_bar + 8 * acc));
+      else
+        mbar_arrive(tempty_bar + 8 * acc);
       if (++acc == 2) {
         acc = 0;
         acc_phase ^= 1u;
@@ -625,8 +708,21 @@ __global__ void __launch_bounds__(192, 1)
 
   tc_fence_before();
   __syncthreads();
+  // Every MMA of the pair has completed once the drain barrier has seen the
+  // leader's final commit; only then may tensor memory be freed and the CTAs
+  // exit (the cluster barrier also keeps each CTA alive while its peer may
+  // still signal its barriers).
+  if (warp == 1 && lane == 0 && !mbar_wait(drain_bar, 0, kDrainNs))
+    record_error(args.err, kErrTimeout);
+  __syncthreads();
+  if constexpr (C::CTA2) cluster_sync();
   tc_fence_after();
-  if (warp == 1) tmem_dealloc(tmem_base, C::TMEM_COLS);
+  if (warp == 1) {
+    if constexpr (C::CTA2)
+      tmem_dealloc2(tmem_base, C::TMEM_COLS);
+    else
+      tmem_dealloc(tmem_base, C::TMEM_COLS);
+  }
 }
 
 template <typename T, int MODE, int BN, int STAGES>
@@ -643,8 +739,19 @@ cudaError_t launch_gemm_t(const GemmMaps& maps, const GemmArgs& args, int num_sm
     if (e != cudaSuccess) return e;
     configured[dev] = true;
   }
-  kern<<<num_sms, 192, C::SMEM_BYTES, st>>>(maps, args);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(num_sms / C::PAIR * C::PAIR));
+  cfg.blockDim = dim3(192);
+  cfg.dynamicSmemBytes = C::SMEM_BYTES;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = C::PAIR;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, maps, args);
 }
 
 }  // namespace moe

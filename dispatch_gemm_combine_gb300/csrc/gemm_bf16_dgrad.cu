@@ -9,7 +9,7 @@ cudaError_t launch_gemm_bf16_dgrad(int mode, const GemmMaps& maps, const GemmArg
   using T = __nv_bfloat16;
   switch (mode) {
     case kDgradDown: return launch_gemm_t<T, kDgradDown, 256, 3>(maps, a, sms, st);
-    case kDgradGateUp: return launch_gemm_t<T, kDgradGateUp, 256, 4>(maps, a, sms, st);
+    case kDgradGateUp: return launch_gemm_t<T, kDgradGateUp, 256, 6>(maps, a, sms, st);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -71,7 +71,9 @@ __device__ int block_exclusive_scan(int v, int* warp_sums, int* total) {
 }
 
 // from_counts = 1: counts[] is given (a caller-built plan) and only the
-// padded offsets are derived; blkhist is not touched.
+// padded offsets are derived; blkhist is not touched.  poff has 2*(E+1)
+// entries: the tile-padded row offsets, then the prefix over experts of
+// their number of 128-row tile pairs (the schedule of the 2-SM GEMMs).
 __global__ void __launch_bounds__(1024) plan_scan_kernel(int* __restrict__ blkhist, int nchunks,
                                                          int E, int* __restrict__ counts,
                                                          int* __restrict__ offsets,
@@ -102,13 +104,18 @@ __global__ void __launch_bounds__(1024) plan_scan_kernel(int* __restrict__ blkhi
   const int padded = (c + kRowTile - 1) / kRowTile * kRowTile;
   int ptot = 0;
   const int pof = block_exclusive_scan(padded, warp_sums, &ptot);
+  const int pairs = (padded / kRowTile + 1) / 2;
+  int pptot = 0;
+  const int ppof = block_exclusive_scan(pairs, warp_sums, &pptot);
   if (e < E) {
     if (!from_counts) offsets[e] = off;
     poff[e] = pof;
+    poff[E + 1 + e] = ppof;
   }
   if (threadIdx.x == 0) {
     if (!from_counts) offsets[E] = totals[0];
     poff[E] = ptot;
+    poff[E + 1 + E] = pptot;
   }
 }
 

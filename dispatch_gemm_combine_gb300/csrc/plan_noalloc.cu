@@ -18,12 +18,13 @@ namespace {
 
 using namespace moe;
 
-// Scratch layout (ints): [0, 64) error word and padding, [64, 64 + 1088)
-// padded offsets (E + 1 <= 1025), then the per-chunk histograms.
+// Scratch layout (ints): [0, 64) error word and padding, [64, 64 + 2112)
+// padded offsets and tile-pair prefix (2 * (E + 1) <= 2050), then the
+// per-chunk histograms.
 constexpr int kScratchInts = 1 << 18;   // 1 MiB
 constexpr int kErrOff = 0;
 constexpr int kPoffOff = 64;
-constexpr int kHistOff = kPoffOff + 1088;
+constexpr int kHistOff = kPoffOff + 2112;
 constexpr int kHistInts = kScratchInts - kHistOff;
 
 static __device__ __align__(256) int g_plan_scratch[kScratchInts];

@@ -170,8 +170,8 @@ const char* moe_status_string(moe_status status);
  * loads the library until the process exits.  This call allocates nothing.
  *   - Arguments and outputs are those of moe_plan, minus the workspace; the
  *     result is identical to moe_plan's.
- *   - Size limit: ceil(T*k / 1024) * E <= 260992 (e.g. T*k <= 1,043,456 for
- *     E = 256, T*k <= 260,096 for E = 1024); larger problems return
+ *   - Size limit: ceil(T*k / 1024) * E <= 259968 (e.g. T*k <= 1,039,360 for
+ *     E = 256, T*k <= 259,072 for E = 1024); larger problems return
  *     MOE_ERR_WORKSPACE without launching anything.
  *   - The first call on a device resolves the device address of the array
  *     (cudaGetSymbolAddress) with that device current; make that first call
