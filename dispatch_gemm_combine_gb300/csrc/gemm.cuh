@@ -240,6 +240,28 @@ __device__ __forceinline__ void store_tile(const OutDesc& o, int b, int r0, int 
   }
 }
 
+// Store a 16-row x 64-column fp32 block read with tmem_ld16x64 straight from
+// registers: lane t writes 8 bytes at rows r0 + t/4 and r0 + 8 + t/4, so four
+// lanes fill one 32-byte sector.  Rows >= o.rows and columns >= o.cols (a
+// multiple of 8) are not written.
+__device__ __forceinline__ void store_rows16(const OutDesc& o, int b, int r0, int c0,
+                                             const float (&v)[32], int lane) {
+  float* base = static_cast<float*>(o.ptr) + static_cast<int64_t>(b) * o.bstride;
+  const int ra = r0 + (lane >> 2), rb = ra + 8;
+  const int cc = c0 + 2 * (lane & 3);
+  float* pa = base + static_cast<int64_t>(ra) * o.ld;
+  float* pb = base + static_cast<int64_t>(rb) * o.ld;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const int col = cc + 8 * j;
+    if (col < o.cols) {
+      if (ra < o.rows) *reinterpret_cast<float2*>(pa + col) = make_float2(v[4 * j], v[4 * j + 1]);
+      if (rb < o.rows)
+        *reinterpret_cast<float2*>(pb + col) = make_float2(v[4 * j + 2], v[4 * j + 3]);
+    }
+  }
+}
+
 __device__ __forceinline__ void split_bf16(float x, float& hi, float& lo) {
   hi = __bfloat162float(__float2bfloat16_rn(x));
   lo = x - hi;
@@ -553,21 +575,20 @@ __global__ void __launch_bounds__(192, 1)
         float v[32];
 
         if constexpr (C::kWgrad) {
+          // fp32 weight gradients go straight from tensor memory to global
+          // memory in 16-row x 64-column blocks
 #pragma unroll 1
-          for (int mc = 0; mc < C::MT * (BN / 64); ++mc) {
-            const int mh = mc / (BN / 64), c = mc % (BN / 64);
-            float w2[64];
+          for (int blk = 0; blk < C::MT * (BN / 64) * 2; ++blk) {
+            const int mh = blk / ((BN / 64) * 2), c = (blk / 2) % (BN / 64), hf = blk & 1;
+            float w2[32];
             if (ti.nkb > 0) {
-              tmem_ld64(tacc + mh * BN + c * 64, w2);
+              tmem_ld16x64(tacc + (static_cast<uint32_t>(hf * 16) << 16) + mh * BN + c * 64, w2);
             } else {
 #pragma unroll
-              for (int i = 0; i < 64; ++i) w2[i] = 0.f;
+              for (int i = 0; i < 32; ++i) w2[i] = 0.f;
             }
-            const int r0 = ti.m0 + mh * 128 + q * 32;
-            store_tile<float>(args.out[0], ti.e, r0, ti.n0 + c * 64,
-                              *reinterpret_cast<const float(*)[32]>(w2), my_epi, lane);
-            store_tile<float>(args.out[0], ti.e, r0, ti.n0 + c * 64 + 32,
-                              *reinterpret_cast<const float(*)[32]>(w2 + 32), my_epi, lane);
+            store_rows16(args.out[0], ti.e, ti.m0 + mh * 128 + q * 32 + hf * 16, ti.n0 + c * 64, w2,
+                         lane);
           }
         } else {
           // routing weight and liveness of this thread's row
