@@ -106,6 +106,7 @@ struct TileInfo {
   int n0;      // first output column
   int m0;      // wgrad: first output row of this CTA
   int nkb;     // k-blocks
+  int klast;   // K rows of the last k-block that can be non-zero
   int nt;      // column-tile index
   bool active; // false when this CTA's 128 rows lie past the expert (or the output)
 };
@@ -128,7 +129,11 @@ __device__ __forceinline__ TileInfo decode_tile(const GemmArgs& a, int t, int bk
     ti.m0 = m * 128 * MT;
     ti.active = m < a.m_tiles;
     ti.row0 = __ldg(a.poff + ti.e);
-    ti.nkb = (__ldg(a.poff + ti.e + 1) - ti.row0) / bk;
+    // contract over the expert's rows only, not over its zero padding: the
+    // k-blocks that hold rows, and in the last of them the MMAs that do
+    const int cnt = min(__ldg(a.counts + ti.e), __ldg(a.poff + ti.e + 1) - ti.row0);
+    ti.nkb = (cnt + bk - 1) / bk;
+    ti.klast = cnt - (ti.nkb - 1) * bk;
   } else {
     // unit prefix of expert e: its tile pairs (PAIR = 2) or tiles (PAIR = 1)
     const int* up = (PAIR == 2) ? a.poff + a.E + 1 : a.poff;
@@ -152,6 +157,7 @@ __device__ __forceinline__ TileInfo decode_tile(const GemmArgs& a, int t, int bk
     ti.row0 = p0 + m * 128;
     ti.m0 = 0;
     ti.nkb = a.num_kb;
+    ti.klast = bk;
   }
   ti.n0 = ti.nt * BN_OUT;
   return ti;
@@ -484,8 +490,13 @@ __global__ void __launch_bounds__(192, 1)
               else
                 tc_mma<C::kTf32>(d_tmem, ad, bd, C::IDESC, accum);
             };
+            // MMAs of this k-block (the last one of a weight gradient may
+            // end early), and whether the second m-tile has output rows
+            const int ksteps = (kb + 1 == ti.nkb) ? (ti.klast + C::MMA_K - 1) / C::MMA_K : C::KSTEPS;
+            const bool mt_live = C::MT > 1 && ti.m0 + 128 < args.out[0].rows;
 #pragma unroll
             for (int kk = 0; kk < C::KSTEPS; ++kk) {
+              if (kk >= ksteps) break;
               const uint32_t aoff = C::A_MN ? kk * C::MMA_K * 128 : kk * 32;
               const uint32_t boff = C::B_MN ? kk * C::MMA_K * 128 : kk * 32;
               const uint32_t albo = C::A_MN ? C::CHUNK_BYTES : 16;
@@ -498,7 +509,7 @@ __global__ void __launch_bounds__(192, 1)
               if constexpr (C::SPLIT_B)
                 mma(adesc, smem_desc_sw128(sB + C::B_PART + boff, blbo, 1024), 1u);
 #pragma unroll
-              for (int mh = 1; mh < C::MT; ++mh) {
+              for (int mh = 1; mh < C::MT && mt_live; ++mh) {
                 // further m-tiles (1-SM only): their own A rows, the same B
                 const uint64_t ad2 = smem_desc_sw128(sA + mh * C::A_PART + aoff, albo, 1024);
                 const uint32_t d2 = d_tmem + mh * BN;
