@@ -579,7 +579,15 @@ __global__ void __launch_bounds__(192, 1)
         break;
       }
       tc_fence_after();
-      if (ti.active) {
+      // Row-grouped modes: a warp whose 32 rows all lie in the expert's
+      // padding has nothing to produce.  Those rows are read later only as
+      // rows of other row-grouped GEMMs (whose results for them are ignored),
+      // never by the combine, the routing-weight reduction or the weight
+      // gradients (whose last MMA step ends inside the warp holding the
+      // expert's last row).
+      const bool warp_rows =
+          C::kWgrad || ti.row0 + q * 32 - __ldg(args.poff + ti.e) < __ldg(args.counts + ti.e);
+      if (ti.active && warp_rows) {
         const uint32_t tacc = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * C::ACC_COLS;
         const int row = ti.row0 + q * 32 + lane;   // row-grouped modes: padded row of this thread
         const int orow = ti.row0 + q * 32;         // first row of this warp's output tiles
