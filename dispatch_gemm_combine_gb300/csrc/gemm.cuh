@@ -307,7 +307,7 @@ __global__ void __launch_bounds__(192, 1)
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(tfull_bar + 8 * s, 1);
-      mbar_init(tempty_bar + 8 * s, 128 * C::PAIR);   // every epilogue thread of the pair
+      mbar_init(tempty_bar + 8 * s, 4 * C::PAIR);   // one lane of every epilogue warp of the pair
     }
     mbar_init(drain_bar, 1);
     fence_barrier_init();
@@ -733,12 +733,16 @@ __global__ void __launch_bounds__(192, 1)
           }
         }
       }
-      // release the accumulator to the MMA issuer (the leader)
+      // release the accumulator to the MMA issuer (the leader): every lane's
+      // tensor-memory reads are ordered before the warp's single arrival
       tc_fence_before();
-      if constexpr (C::CTA2)
-        mbar_arrive_cluster(leader_addr(tempty_bar + 8 * acc));
-      else
-        mbar_arrive(tempty_bar + 8 * acc);
+      __syncwarp();
+      if (lane == 0) {
+        if constexpr (C::CTA2)
+          mbar_arrive_cluster(leader_addr(tempty_bar + 8 * acc));
+        else
+          mbar_arrive(tempty_bar + 8 * acc);
+      }
       if (++acc == 2) {
         acc = 0;
         acc_phase ^= 1u;
