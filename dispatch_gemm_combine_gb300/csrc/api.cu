@@ -43,14 +43,14 @@ cudaError_t launch_gemm(int mode, int elem_bytes, const GemmMaps& maps, const Ge
 // Output-column tile width of each mode (must match the instantiations).
 int gemm_block_n(int mode, int elem_bytes) {
   if (mode == kFwdGateUp) return 128;
-  if (mode == kWgradGateUp && elem_bytes == 2) return 128;
   return 256;
 }
 
-// Output rows per weight-gradient m-tile (two 128-row tiles per CTA for the
-// bf16 gate_up weight gradient).
+// Output rows per weight-gradient m-tile (one CTA's rows).
 int gemm_block_m(int mode, int elem_bytes) {
-  return (mode == kWgradGateUp && elem_bytes == 2) ? 256 : 128;
+  (void)mode;
+  (void)elem_bytes;
+  return 128;
 }
 
 // Rows of the K-major weight box of a dgrad: the bf16 gate_up dgrad runs as

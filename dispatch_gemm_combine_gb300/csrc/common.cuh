@@ -261,6 +261,15 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
                : "memory");
 }
 
+// Arrival on a barrier of another CTA of the cluster with relaxed semantics:
+// it orders none of this thread's earlier memory operations, so, unlike a
+// cluster-scope release, it does not first wait for the thread's
+// outstanding global stores to become visible.
+__device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+               : "memory");
+}
+
 // TMA loads of the 2-SM MMA: the box lands in this CTA's shared memory and
 // the byte count completes on `bar`, which may be the leader CTA's barrier.
 __device__ __forceinline__ void tma_load_2d_g2(uint32_t dst, const CUtensorMap* map, uint32_t bar,

@@ -12,8 +12,10 @@
 // own A rows.  A CTA therefore receives 2/3 of the operand bytes per FLOP
 // of a single-CTA 128 x N tile: the loads of a k-block (A 16 KB + B 16 KB
 // for N=256) then take less time than its MMAs, which a CTA's TMA delivery
-// rate otherwise cannot match.  fp32 storage (TF32
-// products) uses independent CTAs and the 1-SM form.
+// rate otherwise cannot match, and the smaller operand traffic leaves the
+// memory system more room for the epilogues' stores.  The bf16 down dgrad,
+// whose epilogue far outweighs its MMAs, and fp32 storage (TF32 products)
+// use independent CTAs and the 1-SM form.
 //
 // Warp roles: warp 0 = TMA producer, warp 1 = MMA issuer (in the leader)
 // and tensor-memory owner, warps 2..5 = epilogue (warp w reads TMEM lanes
@@ -26,8 +28,9 @@
 // of one expert (the second CTA idles in its epilogue when the expert has an
 // odd number of m-tiles).  Units are ordered (expert, n, m-pair) so the
 // pairs running at the same time share one expert's weight columns in L2.
-// Weight-gradient modes tile the [E, M, N] output and contract over the
-// expert's padded rows (zero-filled padding contributes nothing).
+// Weight-gradient modes tile the [E, M, N] output (a pair: 256 x N) and
+// contract over the expert's rows, stopping at the MMA step that holds its
+// last row (padding rows are zero-filled).
 //
 // Operand layouts (smem, 128-byte swizzle, what TMA writes):
 //   K-major   box {128 B of K, rows}: 8-row groups 1024 B apart (SBO); the
@@ -55,12 +58,11 @@ struct GemmCfg {
   static constexpr int MMA_K = 32 / kES;         // K of one tcgen05.mma
   static constexpr int KSTEPS = BK / MMA_K;      // MMAs per k-block (4)
   static constexpr bool kWgrad = (MODE == kWgradDown || MODE == kWgradGateUp);
-  // 2-SM MMA over a CTA pair for the bf16 forward GEMMs and the gate_up
-  // dgrad; the modes whose epilogue outweighs their MMAs (down dgrad, weight
-  // gradients) keep independent CTAs, as does TF32, since a pair's next MMA
-  // waits for both CTAs' epilogues
+  // 2-SM MMA over a CTA pair for every bf16 mode but the down dgrad, whose
+  // heavy epilogue would hold up both CTAs (a pair's next MMA waits for both
+  // CTAs' epilogues); TF32 keeps independent CTAs
   static constexpr bool CTA2 =
-      !kTf32 && (MODE == kFwdGateUp || MODE == kFwdDown || MODE == kDgradGateUp);
+      !kTf32 && (MODE == kFwdGateUp || MODE == kFwdDown || MODE == kDgradGateUp || kWgrad);
   static constexpr int PAIR = CTA2 ? 2 : 1;
   // TF32 operands must be K-major (the fp32 path transposes the others into
   // the workspace first); 16-bit operands may be MN-major.
@@ -71,13 +73,10 @@ struct GemmCfg {
   // accumulator (about 16 bits of mantissa instead of 8).
   static constexpr bool SPLIT_A = (MODE == kWgradDown) && !kTf32;
   static constexpr bool SPLIT_B = (MODE == kWgradGateUp) && !kTf32;
-  // m-tiles of 128 rows per CTA tile: the bf16 gate_up weight gradient
-  // computes two, so its (split, hence doubled) B tile is loaded once for both
-  static constexpr int MT = (MODE == kWgradGateUp && !kTf32) ? 2 : 1;
   static constexpr int BN_CTA = BN / PAIR;       // B columns held by one CTA
   static constexpr int A_PART = 128 * 128;       // 128 rows of A, one 128-byte K row each
   static constexpr int B_PART = BN_CTA * 128;
-  static constexpr int A_BYTES = A_PART * MT * (SPLIT_A ? 2 : 1);
+  static constexpr int A_BYTES = A_PART * (SPLIT_A ? 2 : 1);
   static constexpr int B_BYTES = B_PART * (SPLIT_B ? 2 : 1);
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;   // per CTA
   static constexpr int CHUNK_BYTES = BK * 128;   // one MN-major box
@@ -89,7 +88,7 @@ struct GemmCfg {
   static constexpr int EPI_BYTES = 4 * (EPI_WARP_BYTES + H1_WARP_BYTES);
   static constexpr int BAR_BYTES = (2 * STAGES + 5) * 8 + 16;
   static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + EPI_BYTES + BAR_BYTES;
-  static constexpr int ACC_COLS = MT * BN;       // TMEM columns of one tile's accumulator(s)
+  static constexpr int ACC_COLS = BN;            // TMEM columns of one tile's accumulator
   static constexpr int TMEM_COLS = (2 * ACC_COLS <= 256) ? 256 : 512;
   // output columns produced per tile (gate_up: BN/2 gate + BN/2 up -> BN/2)
   static constexpr int BN_OUT = (MODE == kFwdGateUp) ? BN / 2 : BN;
@@ -113,8 +112,8 @@ struct TileInfo {
 
 // Work unit t of the schedule.  A unit is PAIR consecutive m-tiles with one
 // column tile; CTA `rank` of the pair takes m-tile unit_m*PAIR+rank (of
-// 128*MT output rows for the weight gradients).
-template <int BN_OUT, bool kWgrad, int PAIR, int MT = 1>
+// 128 output rows for the weight gradients).
+template <int BN_OUT, bool kWgrad, int PAIR>
 __device__ __forceinline__ TileInfo decode_tile(const GemmArgs& a, int t, int bk, int rank) {
   TileInfo ti;
   const int NT = a.n_tiles;
@@ -126,7 +125,7 @@ __device__ __forceinline__ TileInfo decode_tile(const GemmArgs& a, int t, int bk
     const int mp = r / NT;
     ti.nt = r - mp * NT;
     const int m = mp * PAIR + rank;
-    ti.m0 = m * 128 * MT;
+    ti.m0 = m * 128;
     ti.active = m < a.m_tiles;
     ti.row0 = __ldg(a.poff + ti.e);
     // contract over the expert's rows only, not over its zero padding: the
@@ -357,7 +356,7 @@ __global__ void __launch_bounds__(192, 1)
     int64_t issued = 0;
     bool ok = true;
     for (int t = unit0; t < total && ok; t += ustride) {
-      const TileInfo ti = decode_tile<C::BN_OUT, C::kWgrad, C::PAIR, C::MT>(args, t, C::BK, crank);
+      const TileInfo ti = decode_tile<C::BN_OUT, C::kWgrad, C::PAIR>(args, t, C::BK, crank);
       for (int kb = 0; kb < ti.nkb; ++kb) {
         int good = 1;
         if (lane == 0) good = mbar_wait(empty_bar + 8 * stage, phase ^ 1u, tmo);
@@ -393,17 +392,13 @@ __global__ void __launch_bounds__(192, 1)
           } else if constexpr (!C::A_MN) {
             load2(sA, &maps.a, kc, ti.row0);
           } else {
-            // MN-major chunks (128 B of M x BK rows): per m-tile, hi then lo
-            // when split
-            constexpr int NPART = C::SPLIT_A ? 2 : 1;
+            // MN-major chunks (128 B of M x BK rows): hi, then lo when split
 #pragma unroll
-            for (int mh = 0; mh < C::MT; ++mh)
+            for (int part = 0; part < (C::SPLIT_A ? 2 : 1); ++part)
 #pragma unroll
-              for (int part = 0; part < NPART; ++part)
-#pragma unroll
-                for (int c = 0; c < 128 / C::CH; ++c)
-                  load2(sA + (mh * NPART + part) * C::A_PART + c * C::CHUNK_BYTES,
-                        part ? &maps.a2 : &maps.a, ti.m0 + mh * 128 + c * C::CH, ti.row0 + kc);
+              for (int c = 0; c < 128 / C::CH; ++c)
+                load2(sA + part * C::A_PART + c * C::CHUNK_BYTES, part ? &maps.a2 : &maps.a,
+                      ti.m0 + c * C::CH, ti.row0 + kc);
           }
           // ---- B: this CTA's BN_CTA columns
           const int nb = ti.n0 + crank * C::BN_CTA;
@@ -461,7 +456,7 @@ __global__ void __launch_bounds__(192, 1)
       uint32_t acc_phase = 0;
       bool ok = true;
       for (int t = unit0; t < total && ok; t += ustride) {
-        const TileInfo ti = decode_tile<C::BN_OUT, C::kWgrad, C::PAIR, C::MT>(args, t, C::BK, crank);
+        const TileInfo ti = decode_tile<C::BN_OUT, C::kWgrad, C::PAIR>(args, t, C::BK, crank);
         int good = 1;
         if (lane == 0) good = mbar_wait(tempty_bar + 8 * acc, acc_phase ^ 1u, tmo);
         good = __shfl_sync(0xffffffffu, good, 0);
@@ -491,9 +486,8 @@ __global__ void __launch_bounds__(192, 1)
                 tc_mma<C::kTf32>(d_tmem, ad, bd, C::IDESC, accum);
             };
             // MMAs of this k-block (the last one of a weight gradient may
-            // end early), and whether the second m-tile has output rows
+            // end early)
             const int ksteps = (kb + 1 == ti.nkb) ? (ti.klast + C::MMA_K - 1) / C::MMA_K : C::KSTEPS;
-            const bool mt_live = C::MT > 1 && ti.m0 + 128 < args.out[0].rows;
 #pragma unroll
             for (int kk = 0; kk < C::KSTEPS; ++kk) {
               if (kk >= ksteps) break;
@@ -508,16 +502,6 @@ __global__ void __launch_bounds__(192, 1)
                 mma(smem_desc_sw128(sA + C::A_PART + aoff, albo, 1024), bdesc, 1u);
               if constexpr (C::SPLIT_B)
                 mma(adesc, smem_desc_sw128(sB + C::B_PART + boff, blbo, 1024), 1u);
-#pragma unroll
-              for (int mh = 1; mh < C::MT && mt_live; ++mh) {
-                // further m-tiles (1-SM only): their own A rows, the same B
-                const uint64_t ad2 = smem_desc_sw128(sA + mh * C::A_PART + aoff, albo, 1024);
-                const uint32_t d2 = d_tmem + mh * BN;
-                tc_mma<C::kTf32>(d2, ad2, bdesc, C::IDESC, (kb | kk) != 0 ? 1u : 0u);
-                if constexpr (C::SPLIT_B)
-                  tc_mma<C::kTf32>(d2, ad2, smem_desc_sw128(sB + C::B_PART + boff, blbo, 1024),
-                                   C::IDESC, 1u);
-              }
             }
             // the stage is free in both CTAs once these MMAs have read it
             if constexpr (C::CTA2)
@@ -570,7 +554,7 @@ __global__ void __launch_bounds__(192, 1)
     uint32_t acc_phase = 0;
 
     for (int t = unit0; t < total; t += ustride) {
-      const TileInfo ti = decode_tile<C::BN_OUT, C::kWgrad, C::PAIR, C::MT>(args, t, C::BK, crank);
+      const TileInfo ti = decode_tile<C::BN_OUT, C::kWgrad, C::PAIR>(args, t, C::BK, crank);
       int good = 1;
       if (lane == 0) good = mbar_wait(tfull_bar + 8 * acc, acc_phase, tmo);
       good = __shfl_sync(0xffffffffu, good, 0);
@@ -597,17 +581,16 @@ __global__ void __launch_bounds__(192, 1)
           // fp32 weight gradients go straight from tensor memory to global
           // memory in 16-row x 64-column blocks
 #pragma unroll 1
-          for (int blk = 0; blk < C::MT * (BN / 64) * 2; ++blk) {
-            const int mh = blk / ((BN / 64) * 2), c = (blk / 2) % (BN / 64), hf = blk & 1;
+          for (int blk = 0; blk < (BN / 64) * 2; ++blk) {
+            const int c = blk / 2, hf = blk & 1;
             float w2[32];
             if (ti.nkb > 0) {
-              tmem_ld16x64(tacc + (static_cast<uint32_t>(hf * 16) << 16) + mh * BN + c * 64, w2);
+              tmem_ld16x64(tacc + (static_cast<uint32_t>(hf * 16) << 16) + c * 64, w2);
             } else {
 #pragma unroll
               for (int i = 0; i < 32; ++i) w2[i] = 0.f;
             }
-            store_rows16(args.out[0], ti.e, ti.m0 + mh * 128 + q * 32 + hf * 16, ti.n0 + c * 64, w2,
-                         lane);
+            store_rows16(args.out[0], ti.e, ti.m0 + q * 32 + hf * 16, ti.n0 + c * 64, w2, lane);
           }
         } else {
           // routing weight and liveness of this thread's row
@@ -734,12 +717,15 @@ __global__ void __launch_bounds__(192, 1)
         }
       }
       // release the accumulator to the MMA issuer (the leader): every lane's
-      // tensor-memory reads are ordered before the warp's single arrival
+      // tensor-memory reads have completed (tcgen05.wait::ld) and are fenced
+      // before the warp's single arrival.  The arrival orders nothing else:
+      // the odd CTA's remote arrival is relaxed, since a cluster-scope
+      // release would first drain all of the warp's global stores.
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
-        if constexpr (C::CTA2)
-          mbar_arrive_cluster(leader_addr(tempty_bar + 8 * acc));
+        if (C::CTA2 && !leader)
+          mbar_arrive_cluster_relaxed(leader_addr(tempty_bar + 8 * acc));
         else
           mbar_arrive(tempty_bar + 8 * acc);
       }
