@@ -40,6 +40,8 @@
 //             k-th MMA starts k * (MMA K rows) * 128 bytes in.
 #pragma once
 
+#include <type_traits>
+
 #include "kernels.h"
 
 namespace moe {
@@ -162,18 +164,21 @@ __device__ __forceinline__ TileInfo decode_tile(const GemmArgs& a, int t, int bk
   return ti;
 }
 
-template <typename T>
-__device__ __forceinline__ float act_fwd(int act, float g, float u, float L, float alpha) {
-  if (act == 0) return g * sigmoidf_(g) * u;
+// The activation is a template parameter so that the unrolled per-element
+// loops of the epilogues carry no branch: ACT 0 = SwiGLU, 1 = clamped GLU.
+template <int ACT>
+__device__ __forceinline__ float act_fwd(float g, float u, float L, float alpha) {
+  if constexpr (ACT == 0) return g * sigmoidf_(g) * u;
   const float gc = fminf(g, L);
   const float uc = fminf(fmaxf(u, -L), L);
   return (uc + 1.f) * gc * sigmoidf_(alpha * gc);
 }
 
 // a, da/dg, da/du (inclusive clamp masks)
-__device__ __forceinline__ void act_bwd(int act, float g, float u, float L, float alpha, float& a,
+template <int ACT>
+__device__ __forceinline__ void act_bwd(float g, float u, float L, float alpha, float& a,
                                         float& dg, float& du) {
-  if (act == 0) {
+  if constexpr (ACT == 0) {
     const float s = sigmoidf_(g);
     const float sg = g * s;
     a = sg * u;
@@ -605,6 +610,8 @@ __global__ void __launch_bounds__(192, 1)
             }
           }
           if constexpr (MODE == kFwdGateUp) {
+            auto run = [&](auto act_c) {
+            constexpr int ACT = decltype(act_c)::value;
 #pragma unroll 1
             for (int c = 0; c < BN / 64; ++c) {
               float u[32];
@@ -616,11 +623,16 @@ __global__ void __launch_bounds__(192, 1)
               }
 #pragma unroll
               for (int i = 0; i < 32; ++i) {
-                v[i] = act_fwd<T>(args.act, v[i], u[i], args.limit, args.alpha);
+                v[i] = act_fwd<ACT>(v[i], u[i], args.limit, args.alpha);
                 if constexpr (C::kTf32) v[i] = round_tf32(v[i]);   // operand of the down GEMM
               }
               store_tile<T>(args.out[0], 0, orow, ti.n0 + c * 32, v, my_epi, lane);
             }
+            };
+            if (args.act == 0)
+              run(std::integral_constant<int, 0>{});
+            else
+              run(std::integral_constant<int, 1>{});
           } else if constexpr (MODE == kFwdDown || MODE == kDgradGateUp) {
             // fp32 rows for the combine; the down projection also applies the
             // routing weight of the row's slot
@@ -656,6 +668,8 @@ __global__ void __launch_bounds__(192, 1)
             };
             prefetch(0);
             float dot = 0.f;
+            auto run = [&](auto act_c) {
+            constexpr int ACT = decltype(act_c)::value;
 #pragma unroll 1
             for (int c = 0; c < BN / 32; ++c) {
               tmem_ld32(tacc + c * 32, v);   // dA' (before the routing weight)
@@ -673,7 +687,7 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
               for (int i = 0; i < 32; ++i) {
                 float a, pg, pu;
-                act_bwd(args.act, g[i], u[i], args.limit, args.alpha, a, pg, pu);
+                act_bwd<ACT>(g[i], u[i], args.limit, args.alpha, a, pg, pu);
                 dot += v[i] * a;
                 const float da = wrow * v[i];
                 dg[i] = da * pg;
@@ -712,6 +726,11 @@ __global__ void __launch_bounds__(192, 1)
                 store_tile<T>(args.out[5], 0, orow, i0, lo, my_epi, lane);
               }
             }
+            };
+            if (args.act == 0)
+              run(std::integral_constant<int, 0>{});
+            else
+              run(std::integral_constant<int, 1>{});
             args.dwpart[static_cast<int64_t>(ti.nt) * args.rows_max + row] = live ? dot : 0.f;
           }
         }
