@@ -95,6 +95,11 @@ struct GemmCfg {
   // output columns produced per tile (gate_up: BN/2 gate + BN/2 up -> BN/2)
   static constexpr int BN_OUT = (MODE == kFwdGateUp) ? BN / 2 : BN;
   static constexpr uint32_t IDESC = make_idesc(kTf32, A_MN, B_MN, 128 * PAIR, BN);
+  // Row-grouped pairs run an expert's odd last m-tile as one M=128 MMA unit
+  // instead of an M=256 unit with an idle half.  Each CTA then holds 64 rows;
+  // its tensor memory keeps them in lanes 0-63 for columns [0, N/2) and again
+  // in lanes 64-127 for columns [N/2, N), in accumulator columns [0, N/2).
+  static constexpr uint32_t IDESC_HALF = make_idesc(kTf32, A_MN, B_MN, 128, BN);
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
   static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "BN");
   static_assert(2 * ACC_COLS <= 512, "two accumulators must fit in tensor memory");
@@ -110,14 +115,18 @@ struct TileInfo {
   int klast;   // K rows of the last k-block that can be non-zero
   int nt;      // column-tile index
   bool active; // false when this CTA's 128 rows lie past the expert (or the output)
+  bool half;   // row-grouped pair unit of one 128-row tile (64 rows per CTA, M = 128)
 };
 
 // Work unit t of the schedule.  A unit is PAIR consecutive m-tiles with one
 // column tile; CTA `rank` of the pair takes m-tile unit_m*PAIR+rank (of
-// 128 output rows for the weight gradients).
+// 128 output rows for the weight gradients).  In row-grouped pairs, the
+// last unit of an expert with an odd number of m-tiles is a half unit: its
+// one m-tile is split into 64 rows per CTA.
 template <int BN_OUT, bool kWgrad, int PAIR>
 __device__ __forceinline__ TileInfo decode_tile(const GemmArgs& a, int t, int bk, int rank) {
   TileInfo ti;
+  ti.half = false;
   const int NT = a.n_tiles;
   if constexpr (kWgrad) {
     const int MP = (a.m_tiles + PAIR - 1) / PAIR;
@@ -153,9 +162,15 @@ __device__ __forceinline__ TileInfo decode_tile(const GemmArgs& a, int t, int bk
     const int mu = ((__ldg(up + lo + 1) - __ldg(up + lo)) >> sh);   // units of m
     const int local = t - (__ldg(up + lo) >> sh) * NT;
     ti.nt = local / mu;
-    const int m = (local - ti.nt * mu) * PAIR + rank;
+    const int mp = local - ti.nt * mu;
+    const int m = mp * PAIR + rank;
     ti.active = m < mt;
     ti.row0 = p0 + m * 128;
+    if (PAIR == 2 && (mt & 1) && mp == mu - 1) {
+      ti.half = true;
+      ti.active = true;
+      ti.row0 = p0 + (mt - 1) * 128 + rank * 64;
+    }
     ti.m0 = 0;
     ti.nkb = a.num_kb;
     ti.klast = bk;
@@ -408,11 +423,13 @@ __global__ void __launch_bounds__(192, 1)
           // ---- B: this CTA's BN_CTA columns
           const int nb = ti.n0 + crank * C::BN_CTA;
           if constexpr (MODE == kFwdGateUp && C::B_MN) {
-            // the gate half from the even CTA, the up half from the odd one
-            const CUtensorMap* view = crank ? &maps.b1 : &maps.b0;
-#pragma unroll
-            for (int c = 0; c < C::BN_CTA / C::CH; ++c)
-              load3(sB + c * C::CHUNK_BYTES, view, ti.n0 + c * C::CH, kc, ti.e);
+            // each CTA of the pair holds the gate and the up columns of the
+            // same 64 outputs (n0 + 64*rank ...): tile columns are
+            // [gate 0-63 | up 0-63 | gate 64-127 | up 64-127], so that a half
+            // unit's lanes still see gate and up of one output side by side
+            static_assert(C::BN_CTA == 2 * C::CH, "gate_up pair tile: one gate and one up chunk per CTA");
+            load3(sB, &maps.b0, ti.n0 + crank * C::CH, kc, ti.e);
+            load3(sB + C::CHUNK_BYTES, &maps.b1, ti.n0 + crank * C::CH, kc, ti.e);
           } else if constexpr (MODE == kFwdGateUp) {
             // K-major (transposed) weights: gate rows then up rows of the tile
             load3(sB, &maps.b0, kc, ti.n0, ti.e);
@@ -486,7 +503,7 @@ __global__ void __launch_bounds__(192, 1)
             const uint32_t sB = sA + C::A_BYTES;
             auto mma = [&](uint64_t ad, uint64_t bd, uint32_t accum) {
               if constexpr (C::CTA2)
-                tc_mma2(d_tmem, ad, bd, C::IDESC, accum);
+                tc_mma2(d_tmem, ad, bd, ti.half ? C::IDESC_HALF : C::IDESC, accum);
               else
                 tc_mma<C::kTf32>(d_tmem, ad, bd, C::IDESC, accum);
             };
@@ -574,12 +591,15 @@ __global__ void __launch_bounds__(192, 1)
       // never by the combine, the routing-weight reduction or the weight
       // gradients (whose last MMA step ends inside the warp holding the
       // expert's last row).
+      // first tile row of this warp: a half unit's 64 rows per CTA are read
+      // by quarters 0,1 (columns [0, N/2)) and again by 2,3 ([N/2, N))
+      const int rq = ti.half ? (q & 1) * 32 : q * 32;
       const bool warp_rows =
-          C::kWgrad || ti.row0 + q * 32 - __ldg(args.poff + ti.e) < __ldg(args.counts + ti.e);
+          C::kWgrad || ti.row0 + rq - __ldg(args.poff + ti.e) < __ldg(args.counts + ti.e);
       if (ti.active && warp_rows) {
         const uint32_t tacc = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * C::ACC_COLS;
-        const int row = ti.row0 + q * 32 + lane;   // row-grouped modes: padded row of this thread
-        const int orow = ti.row0 + q * 32;         // first row of this warp's output tiles
+        const int row = ti.row0 + rq + lane;   // row-grouped modes: padded row of this thread
+        const int orow = ti.row0 + rq;         // first row of this warp's output tiles
         float v[32];
 
         if constexpr (C::kWgrad) {
@@ -612,11 +632,25 @@ __global__ void __launch_bounds__(192, 1)
           if constexpr (MODE == kFwdGateUp) {
             auto run = [&](auto act_c) {
             constexpr int ACT = decltype(act_c)::value;
+            // output chunks of 32 columns; a half unit's warp takes the two
+            // of its column half
+            const int j0 = ti.half ? (q >> 1) * 2 : 0;
+            const int j1 = ti.half ? j0 + 2 : BN / 64;
 #pragma unroll 1
-            for (int c = 0; c < BN / 64; ++c) {
+            for (int c = j0; c < j1; ++c) {
               float u[32];
-              tmem_ld32(tacc + c * 32, v);
-              tmem_ld32(tacc + BN / 2 + c * 32, u);
+              int gcol, ucol;   // accumulator columns of this chunk's gate and up values
+              if constexpr (C::CTA2) {
+                static_assert(BN == 256, "gate_up pair tile layout");
+                const int tb = ti.half ? 0 : (c >> 1) * 128;
+                gcol = tb + (c & 1) * 32;
+                ucol = gcol + 64;
+              } else {
+                gcol = c * 32;
+                ucol = BN / 2 + c * 32;
+              }
+              tmem_ld32(tacc + gcol, v);
+              tmem_ld32(tacc + ucol, u);
               if (args.save_h1) {
                 store_tile<float>(args.out[1], 0, orow, ti.n0 + c * 32, v, my_epi, lane);
                 store_tile<float>(args.out[2], 0, orow, ti.n0 + c * 32, u, my_epi, lane);
@@ -637,10 +671,14 @@ __global__ void __launch_bounds__(192, 1)
             // fp32 rows for the combine; the down projection also applies the
             // routing weight of the row's slot
             const float scale = (MODE == kFwdDown) ? wrow : 1.f;
+            // 64-column chunks; a half unit's warp takes those of its column
+            // half, held in accumulator columns [0, N/2)
+            const int c0 = ti.half ? (q >> 1) * (BN / 128) : 0;
+            const int c1 = ti.half ? c0 + BN / 128 : BN / 64;
 #pragma unroll 1
-            for (int c = 0; c < BN / 64; ++c) {
+            for (int c = c0; c < c1; ++c) {
               float w2[64];
-              tmem_ld64(tacc + c * 64, w2);
+              tmem_ld64(tacc + (c - (ti.half ? c0 : 0)) * 64, w2);
 #pragma unroll
               for (int i = 0; i < 64; ++i) w2[i] *= scale;
               store_tile<float>(args.out[0], 0, orow, ti.n0 + c * 64,
