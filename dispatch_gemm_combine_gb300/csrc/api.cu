@@ -247,6 +247,17 @@ struct Layout {
 
 int dgrad_down_ntiles(const moe_shape* s) { return (s->I + 255) / 256; }
 
+// The context saved by the training forward: the expert-grouped token rows
+// Xp [rows_max, H] in the storage dtype, then (256-byte aligned) the fp32
+// gate | up pre-activations [rows_max, 2I].
+size_t saved_rows(const moe_shape* s) {
+  const size_t r = static_cast<size_t>(rows_max(s));
+  return r > 0 ? r : 1;
+}
+size_t saved_h1_offset(const moe_shape* s) {
+  return align256(saved_rows(s) * s->H * elem_bytes(s));
+}
+
 Layout layout(const moe_shape* s, int which) {
   Layout L;
   const int64_t Tk = s->T * s->k;
@@ -276,7 +287,6 @@ Layout layout(const moe_shape* s, int which) {
   }
   if (which == 2) {
     L.dyp = take(es * R * s->H);
-    L.xp = take(es * R * s->H);
     L.dh1 = take(es * R * 2 * s->I);
     L.aw = take(es * R * s->I);
     if (es == 2) {  // bf16 remainders of dH1 and w*a (operands of the weight gradients)
@@ -342,8 +352,7 @@ size_t moe_workspace_size(const moe_shape* shape, int which) {
 
 size_t moe_saved_size(const moe_shape* shape) {
   if (!shape_ok(shape)) return 0;
-  const size_t r = static_cast<size_t>(rows_max(shape));
-  return (r > 0 ? r : 1) * 2 * shape->I * sizeof(float);   // fp32 gate | up pre-activations
+  return saved_h1_offset(shape) + saved_rows(shape) * 2 * shape->I * sizeof(float);
 }
 
 uint64_t moe_set_wait_timeout_ns(uint64_t ns) { return g_timeout_ns.exchange(ns); }
@@ -465,8 +474,12 @@ moe_status moe_ffn_fwd(const moe_shape* s, const void* x, const int32_t* topk_id
     perm = p;
     inv = v;
   }
-  void* xp = at<char>(ws, L.xp);
+  // the training forward gathers straight into the saved context, which the
+  // backward reads instead of gathering x again
+  void* xp = saved ? saved : at<char>(ws, L.xp);
   void* aact = at<char>(ws, L.act);
+  float* h1_saved = saved ? reinterpret_cast<float*>(static_cast<char*>(saved) + saved_h1_offset(s))
+                          : nullptr;
   MOE_CUDA(tracked(kKGather, 1, st, [&] {
     return launch_gather_rows(x, H, s->k, E, poff, counts, offsets, perm, static_cast<int>(Tk),
                               R, xp, es, sms, st);
@@ -499,8 +512,8 @@ moe_status moe_ffn_fwd(const moe_shape* s, const void* x, const int32_t* topk_id
   GemmArgs a1 = base_args(s, poff, counts, offsets, perm, topk_w, err);
   a1.out[0] = out_view(aact, I, R, I);
   if (saved) {
-    a1.out[1] = out_view(saved, 2ll * I, R, I);
-    a1.out[2] = out_view(static_cast<float*>(saved) + I, 2ll * I, R, I);
+    a1.out[1] = out_view(h1_saved, 2ll * I, R, I);
+    a1.out[2] = out_view(h1_saved + I, 2ll * I, R, I);
   }
   a1.num_kb = (H + BK - 1) / BK;
   a1.n_tiles = (I + gemm_block_n(kFwdGateUp, es) - 1) / gemm_block_n(kFwdGateUp, es);
@@ -578,7 +591,10 @@ moe_status moe_ffn_bwd(const moe_shape* s, const void* dy, const void* x, const 
   MOE_CUDA(tracked(kKOffsets, 1, st, [&] { return launch_padded_offsets(counts, E, poff, st); }));
 
   void* dyp = at<char>(ws, L.dyp);
-  void* xp = at<char>(ws, L.xp);
+  // the forward's expert-grouped x rows and fp32 pre-activations (saved)
+  void* xp = const_cast<void*>(saved);
+  const float* h1_saved =
+      reinterpret_cast<const float*>(static_cast<const char*>(saved) + saved_h1_offset(s));
   void* dh1 = at<char>(ws, L.dh1);
   void* aw = at<char>(ws, L.aw);
   const bool split = (es == 2);
@@ -588,10 +604,6 @@ moe_status moe_ffn_bwd(const moe_shape* s, const void* dy, const void* x, const 
   MOE_CUDA(tracked(kKGather, 1, st, [&] {
     return launch_gather_rows(dy, H, s->k, E, poff, counts, offsets, perm, static_cast<int>(Tk),
                               R, dyp, es, sms, st);
-  }));
-  MOE_CUDA(tracked(kKGather, 1, st, [&] {
-    return launch_gather_rows(x, H, s->k, E, poff, counts, offsets, perm, static_cast<int>(Tk),
-                              R, xp, es, sms, st);
   }));
 
   const uint32_t BK = 128 / es, CH = 128 / es;
@@ -629,7 +641,7 @@ moe_status moe_ffn_bwd(const moe_shape* s, const void* dy, const void* x, const 
   GemmArgs a1 = base_args(s, poff, counts, offsets, perm, topk_w, err);
   a1.num_kb = (H + BK - 1) / BK;
   a1.n_tiles = dgrad_down_ntiles(s);
-  a1.h1 = saved;
+  a1.h1 = h1_saved;
   a1.dwpart = dwpart;
   a1.out[0] = out_view(dh1, 2ll * I, R, I);
   a1.out[1] = out_view(static_cast<char*>(dh1) + up_off, 2ll * I, R, I);

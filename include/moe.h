@@ -101,10 +101,12 @@ typedef struct {
  * 2 moe_ffn_bwd.  Returns 0 for an invalid shape or `which`. */
 size_t moe_workspace_size(const moe_shape* shape, int which);
 
-/* Bytes of the context the training forward saves for the backward: the
- * gate_up pre-activations in fp32 (whatever the dtype, so the backward sees
- * the accumulator values, not a bf16 rounding of them), in the library's
- * expert-grouped, tile-padded row order.  Returns 0 for an invalid shape. */
+/* Bytes of the context the training forward saves for the backward, in the
+ * library's expert-grouped, tile-padded row order: the gathered token rows
+ * (storage dtype, so the backward does not gather x again), then, 256-byte
+ * aligned, the gate_up pre-activations in fp32 (whatever the dtype, so the
+ * backward sees the accumulator values, not a bf16 rounding of them).
+ * Returns 0 for an invalid shape. */
 size_t moe_saved_size(const moe_shape* shape);
 
 /* Build the dispatch plan of topk_idx [T,k] (int32, device).
@@ -132,8 +134,9 @@ moe_status moe_ffn_fwd(const moe_shape* shape, const void* x,
 
 /* Backward pass of <dy, y>.
  *   dy [T,H]; x, topk_idx, topk_w, w_gate_up, w_down as given to the
- *   forward; plan: the plan of topk_idx (required); saved: the context the
- *   training forward wrote (required).
+ *   forward (x is checked but its rows are read from the saved context);
+ *   plan: the plan of topk_idx (required); saved: the context the training
+ *   forward wrote (required).
  *   Outputs: dx [T,H]; d_topk_w [T,k] fp32; dw_gate_up [E,H,2I] fp32
  *   (d_gate = [:,:,:I], d_up = [:,:,I:]); dw_down [E,I,H] fp32.  Experts
  *   with no routed token get zero weight gradients.  All reductions run in

@@ -41,11 +41,13 @@ def test_workspace_sizes(L):
     bwd = L.moe_workspace_size(s, 2)
     assert fwd >= rows * (2880 + 2880) * 2
     assert bwd >= rows * (2880 * 2 + 2 * 2880 + 2880) * 2
-    assert L.moe_saved_size(s) == rows * 2 * 2880 * 4
+    # saved: the grouped bf16 x rows, then the fp32 gate | up pre-activations
+    assert L.moe_saved_size(s) == rows * 2880 * 2 + rows * 2 * 2880 * 4
     assert L.moe_workspace_size(s, 0) < fwd
     # few tokens: at most Tk experts hold a row
     s2 = L.Shape(3, 64, 64, 256, 2)
-    assert L.moe_saved_size(s2) == (6 + 6 * 127) // 128 * 128 * 2 * 64 * 4
+    rows2 = (6 + 6 * 127) // 128 * 128
+    assert L.moe_saved_size(s2) == rows2 * 64 * 2 + rows2 * 2 * 64 * 4
 
 
 @pytest.mark.parametrize("bad", [dict(H=100), dict(I=12), dict(k=0), dict(E=2, k=3),
