@@ -721,6 +721,16 @@ __global__ void __launch_bounds__(192, 1)
                 g[4 * j] = gv.x; g[4 * j + 1] = gv.y; g[4 * j + 2] = gv.z; g[4 * j + 3] = gv.w;
                 u[4 * j] = uv.x; u[4 * j + 1] = uv.y; u[4 * j + 2] = uv.z; u[4 * j + 3] = uv.w;
               }
+              // refill the staging row with the next chunk as early as possible:
+              // a use of every value read above orders those reads before the
+              // copies that overwrite them
+              if (c + 1 < BN / 32) {
+                float any = 0.f;
+#pragma unroll
+                for (int i = 0; i < 32; ++i) any += g[i] + u[i];
+                asm volatile("" ::"f"(any));
+                prefetch(c + 1);
+              }
               float dg[32], du[32], aw[32];
 #pragma unroll
               for (int i = 0; i < 32; ++i) {
@@ -732,9 +742,6 @@ __global__ void __launch_bounds__(192, 1)
                 du[i] = da * pu;
                 aw[i] = wrow * a;
               }
-              // every value of the staged row is consumed above: refill the
-              // buffer with the next chunk while this one is stored
-              if (c + 1 < BN / 32) prefetch(c + 1);
               if constexpr (C::kTf32) {
                 // operands of the TF32 dgrad / wgrad products
 #pragma unroll
