@@ -678,6 +678,8 @@ moe_status moe_ffn_bwd(const moe_shape* s, const void* dy, const void* x, const 
   m2.b1 = m2.b0;
   GemmArgs a2 = base_args(s, poff, counts, offsets, perm, topk_w, err);
   a2.out[0] = out_view(dw_down, H, I, H, static_cast<int64_t>(I) * H);
+  if (!map3d(&m2.out, 4, dw_down, H, I, E, H, static_cast<int64_t>(I) * H, 32, 32, SW))
+    return MOE_ERR_CUDA;
   a2.m_tiles = (I + 127) / 128;
   a2.n_tiles = (H + gemm_block_n(kWgradDown, es) - 1) / gemm_block_n(kWgradDown, es);
   MOE_CUDA(tracked(kKWgradDown, 1, st, [&] { return launch_gemm(kWgradDown, es, m2, a2, sms, st); }));
@@ -724,6 +726,8 @@ moe_status moe_ffn_bwd(const moe_shape* s, const void* dy, const void* x, const 
   m4.a2 = m4.a;
   GemmArgs a4 = base_args(s, poff, counts, offsets, perm, topk_w, err);
   a4.out[0] = out_view(dw_gate_up, 2ll * I, H, 2ll * I, 2ll * I * H);
+  if (!map3d(&m4.out, 4, dw_gate_up, 2ll * I, H, E, 2ll * I, 2ll * I * H, 32, 32, SW))
+    return MOE_ERR_CUDA;
   a4.m_tiles = (H + gemm_block_m(kWgradGateUp, es) - 1) / gemm_block_m(kWgradGateUp, es);
   a4.n_tiles = (2 * I + bn4 - 1) / bn4;
   MOE_CUDA(tracked(kKWgradGateUp, 1, st, [&] { return launch_gemm(kWgradGateUp, es, m4, a4, sms, st); }));

@@ -85,7 +85,13 @@ struct GemmCfg {
   // per epilogue warp: one 32x32 transpose tile, rows padded to 36 words;
   // the down dgrad also stages the saved pre-activations of its 32 rows
   // (32 gate + 32 up fp32 per row, rows padded to 68 words)
-  static constexpr int EPI_WARP_BYTES = 32 * 36 * 4;
+  // The down weight gradient stores its fp32 tiles with TMA (measured 12%
+  // faster than register stores); the gate_up one, which writes twice the
+  // bytes, keeps register stores (TMA stores measured 2% slower there).
+  static constexpr bool TMA_OUT = (MODE == kWgradDown);
+  // (TMA_OUT: two 32 x 32 fp32 tiles in the 128-byte swizzle, the staging
+  // of the tensor stores)
+  static constexpr int EPI_WARP_BYTES = TMA_OUT ? 2 * 4096 : 32 * 36 * 4;
   static constexpr int H1_WARP_BYTES = (MODE == kDgradDown) ? 32 * 68 * 4 : 0;
   static constexpr int EPI_BYTES = 4 * (EPI_WARP_BYTES + H1_WARP_BYTES);
   static constexpr int BAR_BYTES = (2 * STAGES + 5) * 8 + 16;
@@ -602,7 +608,7 @@ __global__ void __launch_bounds__(192, 1)
         const int orow = ti.row0 + rq;         // first row of this warp's output tiles
         float v[32];
 
-        if constexpr (C::kWgrad) {
+        if constexpr (C::kWgrad && !C::TMA_OUT) {
           // fp32 weight gradients go straight from tensor memory to global
           // memory in 16-row x 64-column blocks
 #pragma unroll 1
@@ -616,6 +622,37 @@ __global__ void __launch_bounds__(192, 1)
               for (int i = 0; i < 32; ++i) w2[i] = 0.f;
             }
             store_rows16(args.out[0], ti.e, ti.m0 + q * 32 + hf * 16, ti.n0 + c * 64, w2, lane);
+          }
+        } else if constexpr (C::kWgrad) {
+          // fp32 weight gradients leave through TMA tensor stores: per 32-column
+          // chunk, lane r writes row r's 128 bytes into a 32 x 32 staging tile
+          // in the 128-byte swizzle (conflict-free 16-byte stores) and one lane
+          // stores the tile; two tiles alternate.  Rows and columns past the
+          // output are clipped by the store.
+          const uint32_t stg = smem_u32(my_epi);
+#pragma unroll 1
+          for (int c = 0; c < BN / 32; ++c) {
+            float w[32];
+            if (ti.nkb > 0) {
+              tmem_ld32(tacc + c * 32, w);
+            } else {
+#pragma unroll
+              for (int i = 0; i < 32; ++i) w[i] = 0.f;
+            }
+            const uint32_t buf = stg + (c & 1) * 4096;
+            // the tile stored from this buffer two chunks ago has been read
+            if (lane == 0) bulk_wait_read<1>();
+            __syncwarp();
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              st_shared_v4(buf + lane * 128 + ((j ^ (lane & 7)) << 4), w[4 * j], w[4 * j + 1],
+                           w[4 * j + 2], w[4 * j + 3]);
+            fence_async_shared();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_3d(&maps.out, buf, ti.n0 + c * 32, ti.m0 + q * 32, ti.e);
+              bulk_commit();
+            }
           }
         } else {
           // routing weight and liveness of this thread's row
@@ -797,6 +834,11 @@ __global__ void __launch_bounds__(192, 1)
         acc = 0;
         acc_phase ^= 1u;
       }
+    }
+    // the weight gradients' tensor stores must be complete before the CTA exits
+    if constexpr (C::TMA_OUT) {
+      if (lane == 0) bulk_wait_all();
+      __syncwarp();
     }
   }
 

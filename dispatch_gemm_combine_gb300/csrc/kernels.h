@@ -90,8 +90,9 @@ struct GemmArgs {
 // a valid map):
 //   a   A operand (hi part when split)      a2  A lo part (split A)
 //   b0  B operand (hi part / gate view)     b1  B lo part (split B) / up view
+//   out weight gradients: the fp32 dW [E, M, N], box {32, 32}, 128B swizzle
 struct GemmMaps {
-  CUtensorMap a, a2, b0, b1;
+  CUtensorMap a, a2, b0, b1, out;
 };
 
 cudaError_t launch_gemm(int mode, int elem_bytes, const GemmMaps& maps, const GemmArgs& args,
