@@ -86,8 +86,10 @@ struct GemmCfg {
   // the down dgrad also stages the saved pre-activations of its 32 rows
   // (32 gate + 32 up fp32 per row, rows padded to 68 words)
   // The down weight gradient stores its fp32 tiles with TMA (measured 12%
-  // faster than register stores); the gate_up one, which writes twice the
-  // bytes, keeps register stores (TMA stores measured 2% slower there).
+  // faster than register stores).  The gate_up one, which writes twice the
+  // bytes, measured 2% slower that way, and the fp32 rows of the forward
+  // down GEMM and the gate_up dgrad measured within 2% of the shared-memory
+  // transposes, so those keep the register paths.
   static constexpr bool TMA_OUT = (MODE == kWgradDown);
   // (TMA_OUT: two 32 x 32 fp32 tiles in the 128-byte swizzle, the staging
   // of the tensor stores)
@@ -290,6 +292,27 @@ __device__ __forceinline__ void store_rows16(const OutDesc& o, int b, int r0, in
       if (rb < o.rows)
         *reinterpret_cast<float2*>(pb + col) = make_float2(v[4 * j + 2], v[4 * j + 3]);
     }
+  }
+}
+
+// Stage lane r's 32 fp32 values as row r of a 32 x 32 tile in the 128-byte
+// swizzle at `buf` (1024-byte aligned; conflict-free 16-byte stores) and
+// store the tile at (x, y, z) of `map` with one TMA tensor store issued by
+// lane 0.  Callers alternate two buffers: the wait keeps at most one earlier
+// store still reading shared memory, i.e. the other buffer's.
+__device__ __forceinline__ void tma_store_tile32(const CUtensorMap* map, uint32_t buf,
+                                                 const float* v, int x, int y, int z, int lane) {
+  if (lane == 0) bulk_wait_read<1>();
+  __syncwarp();
+#pragma unroll
+  for (int j = 0; j < 8; ++j)
+    st_shared_v4(buf + lane * 128 + ((j ^ (lane & 7)) << 4), v[4 * j], v[4 * j + 1], v[4 * j + 2],
+                 v[4 * j + 3]);
+  fence_async_shared();
+  __syncwarp();
+  if (lane == 0) {
+    tma_store_3d(map, buf, x, y, z);
+    bulk_commit();
   }
 }
 
@@ -580,6 +603,13 @@ __global__ void __launch_bounds__(192, 1)
     uint8_t* my_h1 = my_epi + C::EPI_WARP_BYTES;
     int acc = 0;
     uint32_t acc_phase = 0;
+    // TMA_OUT staging: the next of this warp's two 32 x 32 fp32 tiles
+    uint32_t stg_next = 0;
+    auto stg_buf = [&]() -> uint32_t {
+      const uint32_t b = smem_u32(my_epi) + stg_next * 4096;
+      stg_next ^= 1u;
+      return b;
+    };
 
     for (int t = unit0; t < total; t += ustride) {
       const TileInfo ti = decode_tile<C::BN_OUT, C::kWgrad, C::PAIR>(args, t, C::BK, crank);
@@ -629,7 +659,6 @@ __global__ void __launch_bounds__(192, 1)
           // in the 128-byte swizzle (conflict-free 16-byte stores) and one lane
           // stores the tile; two tiles alternate.  Rows and columns past the
           // output are clipped by the store.
-          const uint32_t stg = smem_u32(my_epi);
 #pragma unroll 1
           for (int c = 0; c < BN / 32; ++c) {
             float w[32];
@@ -639,20 +668,7 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
               for (int i = 0; i < 32; ++i) w[i] = 0.f;
             }
-            const uint32_t buf = stg + (c & 1) * 4096;
-            // the tile stored from this buffer two chunks ago has been read
-            if (lane == 0) bulk_wait_read<1>();
-            __syncwarp();
-#pragma unroll
-            for (int j = 0; j < 8; ++j)
-              st_shared_v4(buf + lane * 128 + ((j ^ (lane & 7)) << 4), w[4 * j], w[4 * j + 1],
-                           w[4 * j + 2], w[4 * j + 3]);
-            fence_async_shared();
-            __syncwarp();
-            if (lane == 0) {
-              tma_store_3d(&maps.out, buf, ti.n0 + c * 32, ti.m0 + q * 32, ti.e);
-              bulk_commit();
-            }
+            tma_store_tile32(&maps.out, stg_buf(), w, ti.n0 + c * 32, ti.m0 + q * 32, ti.e, lane);
           }
         } else {
           // routing weight and liveness of this thread's row
