@@ -28,6 +28,9 @@ Conventions (readings where the pages are silent):
   * SwiGLU: a = silu(g) * u.
   * the routing weight scales the expert output after the down projection.
 
+The router step (route) turns logits into top-k ids and weights; the layer
+itself takes ids and weights as given.
+
 Every computation is carried out in float64 on values converted exactly from
 the caller's inputs.  Parity status: every function below is pinned by the
 CPU tests (brute force, closed forms, library special cases, finite
@@ -94,6 +97,31 @@ def activation_grad(g, u, act, limit=CLAMP_LIMIT, alpha=CLAMP_ALPHA):
         du = np.where((u >= -limit) & (u <= limit), gc * s, 0.0)
         return dg, du
     raise ValueError("unknown activation %r" % (act,))
+
+
+def route(logits, k):
+    """Top-k routing of router logits [T, E] (the step before the layer).
+
+    The workload specifications route each token to the k experts with the
+    largest router logits and weight them by a softmax over those k logits;
+    the alternative wording (top-k of the full softmax, renormalised to sum
+    to one) gives the same weights, since the softmax is monotonic and its
+    normaliser cancels.  Readings where the sources are silent: equal logits
+    are ordered by ascending expert id (so the selection is unique), the k
+    choices of a token are listed by descending logit, and the logits are
+    finite.
+
+    Returns topk_idx [T, k] int64 and topk_w [T, k] float64.
+    """
+    z = _f64(logits)
+    T, E = z.shape
+    if not 1 <= k <= E:
+        raise ValueError("need 1 <= k <= E")
+    # stable sort of the negated logits: descending, equal values by id
+    order = np.argsort(-z, axis=1, kind="stable")[:, :k]
+    top = np.take_along_axis(z, order, axis=1)
+    e = np.exp(top - top[:, :1])
+    return order.astype(np.int64), e / e.sum(axis=1, keepdims=True)
 
 
 def dispatch_plan(topk_idx, E):

@@ -411,3 +411,64 @@ def test_backward_empty_experts_and_subset():
     sx, sw, sgu, sd = oracle.moe_backward(dy, x, idx, w, wgu, wd, ACT_SWIGLU, experts=[1, 5])
     np.testing.assert_array_equal(sgu[1], dwgu[1])
     np.testing.assert_array_equal(sd[5], dwd[5])
+
+
+# ------------------------------------------------------------------- router
+def _route_by_selection(z, k):
+    """Top-k by k passes of 'largest remaining logit, lowest id on ties'."""
+    T, E = z.shape
+    idx = np.zeros((T, k), dtype=np.int64)
+    for t in range(T):
+        taken = set()
+        for j in range(k):
+            best = None
+            for e in range(E):
+                if e in taken:
+                    continue
+                if best is None or z[t, e] > z[t, best]:
+                    best = e
+            idx[t, j] = best
+            taken.add(best)
+    return idx
+
+
+@pytest.mark.parametrize("T,E,k,seed", [(40, 8, 2, 0), (25, 16, 5, 1), (12, 7, 7, 2), (30, 32, 8, 3)])
+def test_route_selection_bruteforce(T, E, k, seed):
+    rng = np.random.default_rng(seed)
+    z = rng.normal(size=(T, E)).astype(np.float32)
+    z[:, : E // 2] = np.round(z[:, : E // 2])          # many exact ties
+    idx, w = oracle.route(z, k)
+    assert np.array_equal(idx, _route_by_selection(z.astype(np.float64), k))
+
+
+def test_route_weights_are_renormalised_full_softmax():
+    from scipy.special import softmax
+    rng = np.random.default_rng(4)
+    z = rng.normal(size=(50, 64)) * 3.0
+    idx, w = oracle.route(z, 6)
+    p = softmax(z, axis=1)
+    sel = np.take_along_axis(p, idx, axis=1)
+    np.testing.assert_allclose(w, sel / sel.sum(axis=1, keepdims=True), rtol=1e-12, atol=0)
+    # weights follow the order of the logits and sum to one
+    assert np.all(np.diff(w, axis=1) <= 0)
+    np.testing.assert_allclose(w.sum(axis=1), 1.0, rtol=1e-14)
+
+
+def test_route_special_cases():
+    from scipy.special import softmax
+    rng = np.random.default_rng(5)
+    z = rng.normal(size=(9, 12))
+    idx, w = oracle.route(z, 12)                        # k = E: every expert, full softmax
+    assert all(sorted(r.tolist()) == list(range(12)) for r in idx)
+    np.testing.assert_allclose(w, np.take_along_axis(softmax(z, axis=1), idx, axis=1), rtol=1e-12)
+    i2, w2 = oracle.route(z + 123.25, 4)                # shift invariance
+    i1, w1 = oracle.route(z, 4)
+    assert np.array_equal(i1, i2)
+    np.testing.assert_allclose(w1, w2, rtol=1e-12)
+    ie, we = oracle.route(np.zeros((3, 10)), 4)         # all equal: lowest ids, equal weights
+    assert np.array_equal(ie, np.tile(np.arange(4), (3, 1)))
+    np.testing.assert_allclose(we, 0.25)
+    i0, w0 = oracle.route(np.zeros((2, 1)), 1)          # one expert
+    assert np.array_equal(i0, [[0], [0]]) and np.all(w0 == 1.0)
+    counts, _, _, _ = oracle.dispatch_plan(i1, 12)      # routed ids feed the plan
+    assert counts.sum() == 9 * 4
