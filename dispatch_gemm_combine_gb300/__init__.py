@@ -78,6 +78,8 @@ def lib():
     L.moe_saved_size.restype = ctypes.c_size_t
     L.moe_plan.argtypes = [S, P, PL, P, ctypes.c_size_t, P]
     L.moe_plan.restype = ctypes.c_int
+    L.moe_route.argtypes = [S, P, P, P, PL, P, ctypes.c_size_t, P]
+    L.moe_route.restype = ctypes.c_int
     L.moe_ffn_fwd.argtypes = [S, P, P, P, P, P, PL, P, P, P, ctypes.c_size_t, P]
     L.moe_ffn_fwd.restype = ctypes.c_int
     L.moe_ffn_bwd.argtypes = [S, P, P, P, P, P, P, PL, P, P, P, P, P, P, ctypes.c_size_t, P]
@@ -218,6 +220,14 @@ def workspace(shape, which, device="cuda"):
 def saved_buffer(shape, device="cuda"):
     import torch
     return torch.empty(moe_saved_size(shape), dtype=torch.uint8, device=device)
+
+
+def route(shape, logits, topk_idx, topk_w, plan_struct=None, ws=None, stream=None):
+    """Top-k ids and weights of fp32 logits [T,E] (and the plan, given one)."""
+    _check(lib().moe_route(ctypes.byref(shape), _ptr(logits), _ptr(topk_idx), _ptr(topk_w),
+                           ctypes.byref(plan_struct) if plan_struct is not None else None,
+                           _ptr(ws), 0 if ws is None else ws.numel(), _stream(stream)),
+           "moe_route")
 
 
 def plan(shape, topk_idx, plan_struct, ws, stream=None):

@@ -19,7 +19,7 @@ BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libmoe_gb300.so")
 
 SOURCES = ["api.cu", "plan.cu", "permute.cu", "gemm_bf16_fwd.cu", "gemm_bf16_dgrad.cu",
-           "gemm_bf16_wgrad.cu", "gemm_f32.cu", "plan_noalloc.cu"]
+           "gemm_bf16_wgrad.cu", "gemm_f32.cu", "plan_noalloc.cu", "route.cu"]
 HEADERS = ["common.cuh", "kernels.h", "gemm.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

@@ -73,12 +73,12 @@ std::atomic<uint64_t> g_timeout_ns{2000000000ull};
 // Kernel kinds, for the launch counter and the optional event timer.
 enum Kind : int {
   kKPlan = 0, kKOffsets, kKGather, kKFwdGateUp, kKFwdDown, kKCombine, kKDgradDown, kKDwReduce,
-  kKWgradDown, kKDgradGateUp, kKWgradGateUp, kKMemset, kKTranspose, kNumKinds
+  kKWgradDown, kKDgradGateUp, kKWgradGateUp, kKMemset, kKTranspose, kKRoute, kNumKinds
 };
 const char* const kKindNames[kNumKinds] = {
     "plan", "padded_offsets", "gather_rows", "gemm_fwd_gate_up_act", "gemm_fwd_down_scale",
     "combine", "gemm_dgrad_down_act_bwd", "dw_reduce", "gemm_wgrad_down", "gemm_dgrad_gate_up",
-    "gemm_wgrad_gate_up", "memset", "transpose_f32"};
+    "gemm_wgrad_gate_up", "memset", "transpose_f32", "route"};
 
 std::atomic<uint64_t> g_launches{0};
 std::atomic<int> g_profile{0};
@@ -427,6 +427,27 @@ moe_status moe_plan(const moe_shape* s, const int32_t* topk_idx, const moe_plan_
                        at<int>(ws, L.poff), at<int>(ws, L.blkhist), at<int>(ws, L.err), st);
   }));
   return MOE_OK;
+}
+
+moe_status moe_route(const moe_shape* s, const float* logits, int32_t* topk_idx, float* topk_w,
+                     const moe_plan_t* plan, void* ws, size_t ws_bytes, moe_stream_t stream) {
+  if (!shape_ok(s)) return MOE_ERR_INVALID_ARG;
+  if (plan && (!ws || !plan->counts || !plan->offsets)) return MOE_ERR_INVALID_ARG;
+  const int64_t Tk = s->T * s->k;
+  if (s->T > 0 && (!logits || !topk_idx || !topk_w)) return MOE_ERR_INVALID_ARG;
+  if (plan && Tk > 0 && (!plan->perm || !plan->inv)) return MOE_ERR_INVALID_ARG;
+  if (plan && ws_bytes < layout(s, 0).total) return MOE_ERR_WORKSPACE;
+  int sms = 0;
+  const moe_status ds = device_info(&sms);
+  if (ds != MOE_OK) return ds;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (s->T > 0) {
+    MOE_CUDA(tracked(kKRoute, 1, st, [&] {
+      return launch_route(logits, s->T, s->E, s->k, topk_idx, topk_w, sms, st);
+    }));
+  }
+  if (!plan) return MOE_OK;
+  return moe_plan(s, topk_idx, plan, ws, ws_bytes, stream);
 }
 
 moe_status moe_ffn_fwd(const moe_shape* s, const void* x, const int32_t* topk_idx,

@@ -15,6 +15,12 @@ cudaError_t launch_plan(const int* idx, int64_t Tk, int E, int* counts, int* off
 cudaError_t launch_padded_offsets(const int* counts, int E, int* poff, cudaStream_t st);
 size_t plan_blkhist_ints(int64_t Tk, int E);
 
+// ---- top-k routing (route.cu): topk_idx / topk_w [T,k] from logits [T,E]
+// fp32 (finite); ids by descending logit, equal logits by ascending id;
+// weights are a softmax over the k chosen logits.  E <= 1024, k <= 32.
+cudaError_t launch_route(const float* logits, int64_t T, int E, int k, int* topk_idx,
+                         float* topk_w, int num_sms, cudaStream_t st);
+
 // ---- row movement (permute.cu); elem_bytes is 2 (bf16) or 4 (fp32)
 // dst[p] = src[perm[offsets[e] + p - poff[e]] / k] for the live rows of the
 // tile-padded expert-grouped layout; padding rows (and rows whose slot is

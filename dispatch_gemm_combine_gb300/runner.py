@@ -9,7 +9,7 @@ library's kernels.
 import torch
 
 from . import (MOE_BF16, MOE_FP32, Shape, alloc_plan, check_device_error, ffn_bwd, ffn_fwd,
-               moe_saved_size, plan, workspace)
+               moe_saved_size, plan, route, workspace)
 
 _TORCH_DTYPE = {MOE_BF16: torch.bfloat16, MOE_FP32: torch.float32}
 
@@ -35,6 +35,11 @@ class LayerRunner:
 
     def plan(self, topk_idx, stream=None):
         plan(self.shape, topk_idx, self.plan_s, self.ws_plan, stream)
+
+    def route(self, logits, topk_idx, topk_w, stream=None):
+        """Fill topk_idx [T,k] int32 and topk_w [T,k] fp32 from fp32 logits
+        [T,E] and build the plan of the chosen ids."""
+        route(self.shape, logits, topk_idx, topk_w, self.plan_s, self.ws_plan, stream)
 
     def forward(self, x, topk_idx, topk_w, w_gate_up, w_down, use_plan=True, stream=None):
         """y = layer(x).  With use_plan the plan must have been built by plan();

@@ -116,6 +116,23 @@ moe_status moe_plan(const moe_shape* shape, const int32_t* topk_idx,
                     const moe_plan_t* plan, void* ws, size_t ws_bytes,
                     moe_stream_t stream);
 
+/* Top-k routing, the step before the layer: the layer's inputs topk_idx and
+ * topk_w from router logits.  The pages take the routing as given; the
+ * workload descriptions that accompany them route each token to the k
+ * experts with the largest logits, weighted by the softmax over those k
+ * logits (equivalently, the top-k of the full softmax renormalised to one).
+ *   logits [T,E] fp32 (device, finite); E <= 1024, k <= 32.
+ *   topk_idx [T,k] int32: the chosen ids by descending logit; equal logits
+ *     are taken in ascending expert id, so the choice is unique.
+ *   topk_w [T,k] fp32: softmax over the chosen logits (each row sums to 1).
+ *   plan: NULL, or plan arrays that also receive the dispatch plan of
+ *     topk_idx, exactly as moe_plan builds it (ws: moe_workspace_size(shape,
+ *     0) bytes, required only with a plan).
+ * Outputs are overwritten; T = 0 is a no-op. */
+moe_status moe_route(const moe_shape* shape, const float* logits, int32_t* topk_idx,
+                     float* topk_w, const moe_plan_t* plan, void* ws, size_t ws_bytes,
+                     moe_stream_t stream);
+
 /* Forward pass (dispatch -> gate_up GEMM + activation -> down GEMM with the
  * routing-weight scale -> deterministic k-way combine).
  *   x [T,H], topk_idx [T,k] int32, topk_w [T,k] fp32, w_gate_up [E,H,2I],
