@@ -393,8 +393,21 @@ def main():
     e2e_ms = ranks_max(timed(e2e_step, n_e2e))
     run.check()
 
+
     # ---- accounting
     e_active = int((run.plan_t["counts"] > 0).sum().item())
+
+    # ---- the router step before the layer (not part of the layer metric):
+    # fp32 logits [T, E] -> top-k ids, softmax weights and the plan (it
+    # overwrites the runner's plan, so it runs after the layer's accounting)
+    g = torch.Generator(device="cuda").manual_seed(r.seed)
+    logits = torch.randn(r.T, r.E, device="cuda", generator=g)
+    r_idx = torch.empty((r.T, r.k), dtype=torch.int32, device="cuda")
+    r_w = torch.empty((r.T, r.k), dtype=torch.float32, device="cuda")
+    for _ in range(3):
+        run.route(logits, r_idx, r_w)
+    route_ms = timed(lambda: run.route(logits, r_idx, r_w), 50)
+    run.check()
     f_fwd, f_bwd = layer_flops(r)
     b_fwd, b_bwd = layer_bytes(r, e_active)
     peaks, peak_src = load_peaks()
@@ -466,6 +479,8 @@ def main():
                 "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": int(launches),
+        "router": {"ms": round(route_ms, 4), "what": "moe_route: fp32 logits [T,E] -> top-%d ids, "
+                   "softmax weights and the dispatch plan (outside the layer metric)" % r.k},
         "clocks": clocks.summary(),
         "experts_active": e_active,
     }
