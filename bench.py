@@ -365,6 +365,11 @@ def main():
                                         case.w_down)), n_split)
     bwd_ms = timed(lambda: run.backward(case.dy, case.x, case.topk_idx, case.topk_w,
                                         case.w_gate_up, case.w_down), n_split)
+    # the memory-lean backward: no saved context, recomputed inside
+    run.backward(case.dy, case.x, case.topk_idx, case.topk_w, case.w_gate_up, case.w_down,
+                 recompute=True)
+    bwd_re_ms = timed(lambda: run.backward(case.dy, case.x, case.topk_idx, case.topk_w,
+                                           case.w_gate_up, case.w_down, recompute=True), n_split)
 
     # ---- end to end: pinned host inputs in, per-token results out, every step
     h_in = {n: getattr(case, n).cpu().pin_memory() for n in ("x", "topk_idx", "topk_w", "dy")}
@@ -472,7 +477,8 @@ def main():
                    "T": r.T, "H": r.H, "I": r.I, "E": r.E, "k": r.k, "seed": r.seed,
                    "parallelism": "replicas" if world > 1 else "single GPU",
                    "l2": "no flush: 6.4 GB of expert weights per step exceed the 129 MB L2"},
-        "layer": {"fwd": layer_part(fwd_ms, f_fwd, b_fwd), "bwd": layer_part(bwd_ms, f_bwd, b_bwd)},
+        "layer": {"fwd": layer_part(fwd_ms, f_fwd, b_fwd), "bwd": layer_part(bwd_ms, f_bwd, b_bwd),
+                  "bwd_recompute_ms": round(bwd_re_ms, 4)},
         "roofline": roofline,
         "kernels": per_kernel,
         "e2e": {"value": round(job_throughput(step_flops, world, e2e_ms), 2), "unit": "TFLOP/s",

@@ -209,7 +209,8 @@ def alloc_plan(shape, device="cuda"):
 
 
 def workspace(shape, which, device="cuda"):
-    """Zero-filled workspace for call kind `which` (0 plan, 1 fwd, 2 bwd)."""
+    """Zero-filled workspace for call kind `which` (0 plan, 1 fwd, 2 bwd, 3 bwd
+    without a saved context)."""
     import torch
     n = moe_workspace_size(shape, which)
     if n == 0:

@@ -239,7 +239,7 @@ size_t align256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
 struct Layout {
   size_t err = 0, counts = 0, offsets = 0, perm = 0, inv = 0, poff = 0, blkhist = 0;
   size_t xp = 0, act = 0, ow = 0, dyp = 0, dh1 = 0, dh1lo = 0, aw = 0, awlo = 0, dxp = 0;
-  size_t dwpart = 0;
+  size_t dwpart = 0, h1 = 0;
   // fp32 storage only: K-major copies for the TF32 products
   size_t wguT = 0, wdT = 0, awT = 0, dypT = 0, xpT = 0, dh1T = 0, wdR = 0, wguR = 0;
   size_t total = 0;
@@ -285,7 +285,7 @@ Layout layout(const moe_shape* s, int which) {
       L.wdT = take(sizeof(float) * s->E * static_cast<size_t>(s->I) * s->H);
     }
   }
-  if (which == 2) {
+  if (which == 2 || which == 3) {
     L.dyp = take(es * R * s->H);
     L.dh1 = take(es * R * 2 * s->I);
     L.aw = take(es * R * s->I);
@@ -302,6 +302,11 @@ Layout layout(const moe_shape* s, int which) {
     }
     L.dxp = take(sizeof(float) * R * s->H);
     L.dwpart = take(sizeof(float) * R * dgrad_down_ntiles(s));
+  }
+  if (which == 3) {   // backward without a saved context: recompute it
+    L.xp = take(es * R * s->H);
+    L.h1 = take(sizeof(float) * R * 2 * s->I);
+    if (es == 4) L.wguT = take(sizeof(float) * s->E * 2ull * s->I * s->H);
   }
   L.total = off;
   return L;
@@ -340,13 +345,57 @@ GemmArgs base_args(const moe_shape* s, const int* poff, const int* counts, const
   return a;
 }
 
+// gate_up GEMM + activation on the grouped rows xp: the activation into
+// aact [R, I] and, when h1 is given, the fp32 pre-activations [R, 2I]
+// (gate | up).  fp32 storage first transposes the weights into wguT.
+moe_status enqueue_gate_up(const moe_shape* s, const void* xp, const void* w_gate_up, float* wguT,
+                           void* aact, float* h1, int* poff, const int* counts,
+                           const int* offsets, const int* perm, const float* topk_w, int* err,
+                           int sms, cudaStream_t st) {
+  const int es = elem_bytes(s);
+  const int64_t R = rows_max(s);
+  const int H = s->H, I = s->I, E = s->E;
+  const uint32_t BK = 128 / es, CH = 128 / es;
+  const auto SW = CU_TENSOR_MAP_SWIZZLE_128B;
+  const char* wgu = static_cast<const char*>(w_gate_up);
+  GemmMaps m1;
+  const uint32_t AROWS = 128;
+  bool ok = map2d(&m1.a, es, xp, H, R, H, BK, AROWS, SW);
+  if (es == 2) {
+    ok = ok && map3d(&m1.b0, es, wgu, I, H, E, 2ll * I, 2ll * I * H, CH, BK, SW) &&
+         map3d(&m1.b1, es, wgu + static_cast<size_t>(I) * es, I, H, E, 2ll * I, 2ll * I * H, CH,
+               BK, SW);
+  } else {
+    // TF32 takes K-major operands only: use the transposed weights [E, 2I, H]
+    MOE_CUDA(tracked(kKTranspose, 1, st, [&] {
+      return launch_transpose_f32(static_cast<const float*>(w_gate_up), wguT, E, H, 2 * I, st);
+    }));
+    ok = ok && map3d(&m1.b0, es, wguT, H, I, E, H, 2ll * I * H, BK, 128, SW) &&
+         map3d(&m1.b1, es, wguT + static_cast<size_t>(I) * H, H, I, E, H, 2ll * I * H, BK, 128,
+               SW);
+  }
+  if (!ok) return MOE_ERR_CUDA;
+  m1.a2 = m1.a;
+  GemmArgs a1 = base_args(s, poff, counts, offsets, perm, topk_w, err);
+  a1.out[0] = out_view(aact, I, R, I);
+  if (h1) {
+    a1.out[1] = out_view(h1, 2ll * I, R, I);
+    a1.out[2] = out_view(h1 + I, 2ll * I, R, I);
+  }
+  a1.num_kb = (H + BK - 1) / BK;
+  a1.n_tiles = (I + gemm_block_n(kFwdGateUp, es) - 1) / gemm_block_n(kFwdGateUp, es);
+  a1.save_h1 = h1 ? 1 : 0;
+  MOE_CUDA(tracked(kKFwdGateUp, 1, st, [&] { return launch_gemm(kFwdGateUp, es, m1, a1, sms, st); }));
+  return MOE_OK;
+}
+
 }  // namespace
 
 // ====================================================================== ABI
 extern "C" {
 
 size_t moe_workspace_size(const moe_shape* shape, int which) {
-  if (!shape_ok(shape) || which < 0 || which > 2) return 0;
+  if (!shape_ok(shape) || which < 0 || which > 3) return 0;
   return layout(shape, which).total;
 }
 
@@ -506,45 +555,19 @@ moe_status moe_ffn_fwd(const moe_shape* s, const void* x, const int32_t* topk_id
                               R, xp, es, sms, st);
   }));
 
+  const moe_status gs = enqueue_gate_up(s, xp, w_gate_up, es == 4 ? at<float>(ws, L.wguT) : nullptr,
+                                        aact, h1_saved, poff, counts, offsets, perm, topk_w, err,
+                                        sms, st);
+  if (gs != MOE_OK) return gs;
+
   const uint32_t BK = 128 / es, CH = 128 / es;
   const auto SW = CU_TENSOR_MAP_SWIZZLE_128B;
-  const char* wgu = static_cast<const char*>(w_gate_up);
-
-  // gate_up GEMM + activation (+ fp32 pre-activations saved for the backward)
-  GemmMaps m1;
   const uint32_t AROWS = 128;
-  bool ok = map2d(&m1.a, es, xp, H, R, H, BK, AROWS, SW);
-  if (es == 2) {
-    ok = ok && map3d(&m1.b0, es, wgu, I, H, E, 2ll * I, 2ll * I * H, CH, BK, SW) &&
-         map3d(&m1.b1, es, wgu + static_cast<size_t>(I) * es, I, H, E, 2ll * I, 2ll * I * H, CH,
-               BK, SW);
-  } else {
-    // TF32 takes K-major operands only: use the transposed weights [E, 2I, H]
-    float* wguT = at<float>(ws, L.wguT);
-    MOE_CUDA(tracked(kKTranspose, 1, st, [&] {
-      return launch_transpose_f32(static_cast<const float*>(w_gate_up), wguT, E, H, 2 * I, st);
-    }));
-    ok = ok && map3d(&m1.b0, es, wguT, H, I, E, H, 2ll * I * H, BK, 128, SW) &&
-         map3d(&m1.b1, es, wguT + static_cast<size_t>(I) * H, H, I, E, H, 2ll * I * H, BK, 128,
-               SW);
-  }
-  if (!ok) return MOE_ERR_CUDA;
-  m1.a2 = m1.a;
-  GemmArgs a1 = base_args(s, poff, counts, offsets, perm, topk_w, err);
-  a1.out[0] = out_view(aact, I, R, I);
-  if (saved) {
-    a1.out[1] = out_view(h1_saved, 2ll * I, R, I);
-    a1.out[2] = out_view(h1_saved + I, 2ll * I, R, I);
-  }
-  a1.num_kb = (H + BK - 1) / BK;
-  a1.n_tiles = (I + gemm_block_n(kFwdGateUp, es) - 1) / gemm_block_n(kFwdGateUp, es);
-  a1.save_h1 = saved ? 1 : 0;
-  MOE_CUDA(tracked(kKFwdGateUp, 1, st, [&] { return launch_gemm(kFwdGateUp, es, m1, a1, sms, st); }));
 
   // down GEMM * routing weight -> fp32 rows Ow
   float* ow = at<float>(ws, L.ow);
   GemmMaps m2;
-  ok = map2d(&m2.a, es, aact, I, R, I, BK, AROWS, SW);
+  bool ok = map2d(&m2.a, es, aact, I, R, I, BK, AROWS, SW);
   if (es == 2) {
     ok = ok && map3d(&m2.b0, es, w_down, H, I, E, H, static_cast<int64_t>(H) * I, CH, BK, SW);
   } else {
@@ -591,14 +614,16 @@ moe_status moe_ffn_bwd(const moe_shape* s, const void* dy, const void* x, const 
     }));
     return MOE_OK;
   }
-  if (!dy || !x || !topk_idx || !topk_w || !plan || !saved || !dx || !d_topk_w)
+  if (!dy || !x || !topk_idx || !topk_w || !plan || !dx || !d_topk_w)
     return MOE_ERR_INVALID_ARG;
   if (!plan->counts || !plan->offsets || !plan->perm || !plan->inv) return MOE_ERR_INVALID_ARG;
-  if (!aligned16(dy) || !aligned16(x) || !aligned16(dx) || !aligned16(saved) ||
+  if (!aligned16(dy) || !aligned16(x) || !aligned16(dx) || (saved && !aligned16(saved)) ||
       !aligned16(w_gate_up) || !aligned16(w_down) || !aligned16(dw_gate_up) ||
       !aligned16(dw_down))
     return MOE_ERR_INVALID_ARG;
-  const Layout L = layout(s, 2);
+  // without a saved context the backward recomputes it (workspace kind 3)
+  const bool recompute = (saved == nullptr);
+  const Layout L = layout(s, recompute ? 3 : 2);
   if (ws_bytes < L.total) return MOE_ERR_WORKSPACE;
 
   const int64_t Tk = s->T * s->k;
@@ -612,10 +637,13 @@ moe_status moe_ffn_bwd(const moe_shape* s, const void* dy, const void* x, const 
   MOE_CUDA(tracked(kKOffsets, 1, st, [&] { return launch_padded_offsets(counts, E, poff, st); }));
 
   void* dyp = at<char>(ws, L.dyp);
-  // the forward's expert-grouped x rows and fp32 pre-activations (saved)
-  void* xp = const_cast<void*>(saved);
+  // the forward's expert-grouped x rows and fp32 pre-activations: saved, or
+  // recomputed here by the forward's gather and gate_up GEMM (bit-identical)
+  void* xp = recompute ? at<char>(ws, L.xp) : const_cast<void*>(saved);
   const float* h1_saved =
-      reinterpret_cast<const float*>(static_cast<const char*>(saved) + saved_h1_offset(s));
+      recompute ? at<float>(ws, L.h1)
+                : reinterpret_cast<const float*>(static_cast<const char*>(saved) +
+                                                 saved_h1_offset(s));
   void* dh1 = at<char>(ws, L.dh1);
   void* aw = at<char>(ws, L.aw);
   const bool split = (es == 2);
@@ -626,6 +654,19 @@ moe_status moe_ffn_bwd(const moe_shape* s, const void* dy, const void* x, const 
     return launch_gather_rows(dy, H, s->k, E, poff, counts, offsets, perm, static_cast<int>(Tk),
                               R, dyp, es, sms, st);
   }));
+  if (recompute) {
+    MOE_CUDA(tracked(kKGather, 1, st, [&] {
+      return launch_gather_rows(x, H, s->k, E, poff, counts, offsets, perm, static_cast<int>(Tk),
+                                R, xp, es, sms, st);
+    }));
+    // the activation output is not needed: it goes to the dH1 region, which
+    // the down dgrad overwrites
+    const moe_status gs =
+        enqueue_gate_up(s, xp, w_gate_up, es == 4 ? at<float>(ws, L.wguT) : nullptr, dh1,
+                        const_cast<float*>(h1_saved), poff, counts, offsets, perm, topk_w, err,
+                        sms, st);
+    if (gs != MOE_OK) return gs;
+  }
 
   const uint32_t BK = 128 / es, CH = 128 / es;
   const auto SW = CU_TENSOR_MAP_SWIZZLE_128B;

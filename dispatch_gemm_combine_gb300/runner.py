@@ -48,9 +48,19 @@ class LayerRunner:
                 self.plan_s if use_plan else None, self.saved, stream)
         return self.y
 
-    def backward(self, dy, x, topk_idx, topk_w, w_gate_up, w_down, stream=None):
-        ffn_bwd(self.shape, dy, x, topk_idx, topk_w, w_gate_up, w_down, self.plan_s, self.saved,
-                self.dx, self.d_topk_w, self.dw_gate_up, self.dw_down, self.ws_bwd, stream)
+    def backward(self, dy, x, topk_idx, topk_w, w_gate_up, w_down, stream=None, recompute=False):
+        """Gradients of <dy, y>.  With recompute the saved context is not used:
+        the backward recomputes it in a larger workspace (allocated on first use)."""
+        if recompute:
+            if getattr(self, "ws_bwd_recompute", None) is None:
+                self.ws_bwd_recompute = workspace(self.shape, 3, self.device)
+            ffn_bwd(self.shape, dy, x, topk_idx, topk_w, w_gate_up, w_down, self.plan_s, None,
+                    self.dx, self.d_topk_w, self.dw_gate_up, self.dw_down, self.ws_bwd_recompute,
+                    stream)
+        else:
+            ffn_bwd(self.shape, dy, x, topk_idx, topk_w, w_gate_up, w_down, self.plan_s,
+                    self.saved, self.dx, self.d_topk_w, self.dw_gate_up, self.dw_down,
+                    self.ws_bwd, stream)
         return self.dx, self.d_topk_w, self.dw_gate_up, self.dw_down
 
     def check(self, stream=None):

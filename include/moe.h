@@ -97,8 +97,10 @@ typedef struct {
   int32_t* inv;
 } moe_plan_t;
 
-/* Bytes of workspace needed by one call: which = 0 moe_plan, 1 moe_ffn_fwd,
- * 2 moe_ffn_bwd.  Returns 0 for an invalid shape or `which`. */
+/* Bytes of workspace needed by one call: which = 0 moe_plan (and
+ * moe_route with a plan), 1 moe_ffn_fwd, 2 moe_ffn_bwd with a saved
+ * context, 3 moe_ffn_bwd without one (it then recomputes the context).
+ * Returns 0 for an invalid shape or `which`. */
 size_t moe_workspace_size(const moe_shape* shape, int which);
 
 /* Bytes of the context the training forward saves for the backward, in the
@@ -151,9 +153,13 @@ moe_status moe_ffn_fwd(const moe_shape* shape, const void* x,
 
 /* Backward pass of <dy, y>.
  *   dy [T,H]; x, topk_idx, topk_w, w_gate_up, w_down as given to the
- *   forward (x is checked but its rows are read from the saved context);
- *   plan: the plan of topk_idx (required); saved: the context the training
- *   forward wrote (required).
+ *   forward; plan: the plan of topk_idx (required).
+ *   saved: the context the training forward wrote, or NULL.  With NULL the
+ *   backward recomputes the context (the forward's gather of x and its
+ *   gate_up GEMM, one third of the forward's FLOPs) into a workspace of
+ *   moe_workspace_size(shape, 3) bytes; the results are bit-identical to
+ *   those with the saved context, which needs moe_saved_size() bytes of
+ *   caller memory between the two calls instead.
  *   Outputs: dx [T,H]; d_topk_w [T,k] fp32; dw_gate_up [E,H,2I] fp32
  *   (d_gate = [:,:,:I], d_up = [:,:,I:]); dw_down [E,I,H] fp32.  Experts
  *   with no routed token get zero weight gradients.  All reductions run in

@@ -44,6 +44,10 @@ def test_workspace_sizes(L):
     # saved: the grouped bf16 x rows, then the fp32 gate | up pre-activations
     assert L.moe_saved_size(s) == rows * 2880 * 2 + rows * 2 * 2880 * 4
     assert L.moe_workspace_size(s, 0) < fwd
+    # a backward without the saved context also holds the grouped x rows and
+    # the fp32 pre-activations it recomputes
+    assert L.moe_workspace_size(s, 3) >= bwd + rows * 2880 * 2 + rows * 2 * 2880 * 4
+    assert L.moe_workspace_size(s, 4) == 0
     # few tokens: at most Tk experts hold a row
     s2 = L.Shape(3, 64, 64, 256, 2)
     rows2 = (6 + 6 * 127) // 128 * 128

@@ -162,3 +162,22 @@ def test_zero_tokens():
     torch.cuda.synchronize()
     run.check()
     assert torch.all(run.dw_gate_up == 0) and torch.all(run.dw_down == 0)
+
+
+@pytest.mark.parametrize("act,dtype", [(ACT_CLAMPED_GLU, "bf16"), (ACT_SWIGLU, "fp32")])
+def test_backward_recompute_is_bit_identical(act, dtype):
+    """Without the saved context the backward recomputes it with the same
+    kernels on the same inputs, so every gradient must match bit for bit."""
+    r = _recipe(700, 136, 200, 8, 3, act, seed=21, dtype=dtype)
+    case = to_device(synth.make_case(r))
+    run = _runner(r)
+    run.plan(case.topk_idx)
+    run.forward(case.x, case.topk_idx, case.topk_w, case.w_gate_up, case.w_down)
+    saved = [t.clone() for t in run.backward(case.dy, case.x, case.topk_idx, case.topk_w,
+                                             case.w_gate_up, case.w_down)]
+    again = run.backward(case.dy, case.x, case.topk_idx, case.topk_w, case.w_gate_up,
+                         case.w_down, recompute=True)
+    torch.cuda.synchronize()
+    run.check()
+    for name, a, b in zip(("dx", "d_topk_w", "dw_gate_up", "dw_down"), saved, again):
+        assert torch.equal(a, b), name
