@@ -32,6 +32,8 @@ MOE_ERR_TIMEOUT = 5
 MOE_ERR_CUDA = 6
 MOE_ACT_SWIGLU = 0
 MOE_ACT_CLAMPED_GLU = 1
+MOE_GATE_UP_CONCAT = 0
+MOE_GATE_UP_INTERLEAVED = 1
 MOE_BF16 = 0
 MOE_FP32 = 1
 
@@ -43,7 +45,7 @@ class MoeShape(ctypes.Structure):
     _fields_ = [("T", ctypes.c_int64), ("H", ctypes.c_int32), ("I", ctypes.c_int32),
                 ("E", ctypes.c_int32), ("k", ctypes.c_int32), ("act", ctypes.c_int32),
                 ("clamp_limit", ctypes.c_float), ("alpha", ctypes.c_float),
-                ("dtype", ctypes.c_int32)]
+                ("dtype", ctypes.c_int32), ("gate_up_layout", ctypes.c_int32)]
 
 
 class MoePlan(ctypes.Structure):
@@ -176,8 +178,9 @@ def moe_plan_noalloc(shape, topk_idx, plan, stream):
 
 
 # ---------------------------------------------------------------- torch helpers
-def Shape(T, H, I, E, k, act=MOE_ACT_SWIGLU, dtype=MOE_BF16, clamp_limit=7.0, alpha=1.702):
-    return MoeShape(T, H, I, E, k, act, clamp_limit, alpha, dtype)
+def Shape(T, H, I, E, k, act=MOE_ACT_SWIGLU, dtype=MOE_BF16, clamp_limit=7.0, alpha=1.702,
+          gate_up_layout=0):
+    return MoeShape(T, H, I, E, k, act, clamp_limit, alpha, dtype, gate_up_layout)
 
 
 def _ptr(t):

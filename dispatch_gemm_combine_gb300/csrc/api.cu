@@ -221,6 +221,8 @@ bool shape_ok(const moe_shape* s) {
   if (s->k < 1 || s->k > kMaxTopK || s->E < s->k || s->E > kMaxExperts) return false;
   if (s->act != MOE_ACT_SWIGLU && s->act != MOE_ACT_CLAMPED_GLU) return false;
   if (s->dtype != MOE_BF16 && s->dtype != MOE_FP32) return false;
+  if (s->gate_up_layout != MOE_GATE_UP_CONCAT && s->gate_up_layout != MOE_GATE_UP_INTERLEAVED)
+    return false;
   if (s->T * static_cast<int64_t>(s->k) >= (1ll << 31)) return false;
   return true;
 }
@@ -336,6 +338,7 @@ GemmArgs base_args(const moe_shape* s, const int* poff, const int* counts, const
   a.tk = static_cast<int>(s->T * s->k);
   a.E = s->E;
   a.act = s->act;
+  a.gu_interleaved = s->gate_up_layout == MOE_GATE_UP_INTERLEAVED ? 1 : 0;
   a.limit = s->clamp_limit;
   a.alpha = s->alpha;
   a.I = s->I;
@@ -360,19 +363,27 @@ moe_status enqueue_gate_up(const moe_shape* s, const void* xp, const void* w_gat
   const char* wgu = static_cast<const char*>(w_gate_up);
   GemmMaps m1;
   const uint32_t AROWS = 128;
+  const bool il = s->gate_up_layout == MOE_GATE_UP_INTERLEAVED;
   bool ok = map2d(&m1.a, es, xp, H, R, H, BK, AROWS, SW);
-  if (es == 2) {
+  if (es == 2 && il) {
+    // interleaved columns: one view of all 2I columns (the kernel loads the
+    // gate/up pairs of its outputs as consecutive columns)
+    ok = ok && map3d(&m1.b0, es, wgu, 2ll * I, H, E, 2ll * I, 2ll * I * H, CH, BK, SW);
+    m1.b1 = m1.b0;
+  } else if (es == 2) {
     ok = ok && map3d(&m1.b0, es, wgu, I, H, E, 2ll * I, 2ll * I * H, CH, BK, SW) &&
          map3d(&m1.b1, es, wgu + static_cast<size_t>(I) * es, I, H, E, 2ll * I, 2ll * I * H, CH,
                BK, SW);
   } else {
-    // TF32 takes K-major operands only: use the transposed weights [E, 2I, H]
+    // TF32 takes K-major operands only: use the transposed weights [E, 2I, H];
+    // gate rows are [0, I) (concatenated) or the even rows (interleaved)
     MOE_CUDA(tracked(kKTranspose, 1, st, [&] {
       return launch_transpose_f32(static_cast<const float*>(w_gate_up), wguT, E, H, 2 * I, st);
     }));
-    ok = ok && map3d(&m1.b0, es, wguT, H, I, E, H, 2ll * I * H, BK, 128, SW) &&
-         map3d(&m1.b1, es, wguT + static_cast<size_t>(I) * H, H, I, E, H, 2ll * I * H, BK, 128,
-               SW);
+    const int64_t rstride = il ? 2ll * H : H;
+    const size_t up0 = il ? static_cast<size_t>(H) : static_cast<size_t>(I) * H;
+    ok = ok && map3d(&m1.b0, es, wguT, H, I, E, rstride, 2ll * I * H, BK, 128, SW) &&
+         map3d(&m1.b1, es, wguT + up0, H, I, E, rstride, 2ll * I * H, BK, 128, SW);
   }
   if (!ok) return MOE_ERR_CUDA;
   m1.a2 = m1.a;
@@ -705,10 +716,12 @@ moe_status moe_ffn_bwd(const moe_shape* s, const void* dy, const void* x, const 
   a1.n_tiles = dgrad_down_ntiles(s);
   a1.h1 = h1_saved;
   a1.dwpart = dwpart;
-  a1.out[0] = out_view(dh1, 2ll * I, R, I);
+  // interleaved gate_up columns: dgate / dup pairs over all 2I columns
+  const bool il = s->gate_up_layout == MOE_GATE_UP_INTERLEAVED;
+  a1.out[0] = out_view(dh1, 2ll * I, R, il ? 2ll * I : I);
   a1.out[1] = out_view(static_cast<char*>(dh1) + up_off, 2ll * I, R, I);
   a1.out[2] = out_view(aw, I, R, I);
-  a1.out[3] = out_view(dh1lo, 2ll * I, R, I);
+  a1.out[3] = out_view(dh1lo, 2ll * I, R, il ? 2ll * I : I);
   a1.out[4] = out_view(static_cast<char*>(dh1lo) + up_off, 2ll * I, R, I);
   a1.out[5] = out_view(awlo, I, R, I);
   MOE_CUDA(tracked(kKDgradDown, 1, st, [&] { return launch_gemm(kDgradDown, es, m1, a1, sms, st); }));

@@ -51,7 +51,7 @@ namespace moe {
 // that a CTA never exits with asynchronous work still writing its memory.
 constexpr uint64_t kDrainNs = 1000000000ull;
 
-template <typename T, int MODE, int BN, int STAGES>
+template <typename T, int MODE, int BN, int STAGES, bool IL_ = false>
 struct GemmCfg {
   static constexpr int kES = sizeof(T);
   static constexpr bool kTf32 = (kES == 4);
@@ -60,6 +60,11 @@ struct GemmCfg {
   static constexpr int MMA_K = 32 / kES;         // K of one tcgen05.mma
   static constexpr int KSTEPS = BK / MMA_K;      // MMAs per k-block (4)
   static constexpr bool kWgrad = (MODE == kWgradDown || MODE == kWgradGateUp);
+  // interleaved gate_up columns (gate = even, up = odd): a separate
+  // instantiation of the two modes that see the layout (the gate_up forward
+  // and the down dgrad), so the concatenated kernels are unchanged
+  static constexpr bool IL = IL_;
+  static_assert(!IL || MODE == kFwdGateUp || MODE == kDgradDown, "layout-specific modes only");
   // 2-SM MMA over a CTA pair for every bf16 mode but the down dgrad, whose
   // heavy epilogue would hold up both CTAs (a pair's next MMA waits for both
   // CTAs' epilogues); TF32 keeps independent CTAs
@@ -316,15 +321,19 @@ __device__ __forceinline__ void tma_store_tile32(const CUtensorMap* map, uint32_
   }
 }
 
+__device__ __forceinline__ float bf16_round(float x) {
+  return __bfloat162float(__float2bfloat16_rn(x));
+}
+
 __device__ __forceinline__ void split_bf16(float x, float& hi, float& lo) {
-  hi = __bfloat162float(__float2bfloat16_rn(x));
+  hi = bf16_round(x);
   lo = x - hi;
 }
 
-template <typename T, int MODE, int BN, int STAGES>
+template <typename T, int MODE, int BN, int STAGES, bool IL>
 __global__ void __launch_bounds__(192, 1)
     moe_gemm_kernel(const __grid_constant__ GemmMaps maps, const __grid_constant__ GemmArgs args) {
-  using C = GemmCfg<T, MODE, BN, STAGES>;
+  using C = GemmCfg<T, MODE, BN, STAGES, IL>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t sbase = (raw + 1023u) & ~1023u;
@@ -457,8 +466,17 @@ __global__ void __launch_bounds__(192, 1)
             // [gate 0-63 | up 0-63 | gate 64-127 | up 64-127], so that a half
             // unit's lanes still see gate and up of one output side by side
             static_assert(C::BN_CTA == 2 * C::CH, "gate_up pair tile: one gate and one up chunk per CTA");
-            load3(sB, &maps.b0, ti.n0 + crank * C::CH, kc, ti.e);
-            load3(sB + C::CHUNK_BYTES, &maps.b1, ti.n0 + crank * C::CH, kc, ti.e);
+            if constexpr (C::IL) {
+              // interleaved columns (maps.b0 views all 2I): the 128
+              // consecutive columns 2*(n0 + 64*rank) ... hold the gate/up
+              // pairs of this CTA's 64 outputs
+              const int col = 2 * (ti.n0 + crank * C::CH);
+              load3(sB, &maps.b0, col, kc, ti.e);
+              load3(sB + C::CHUNK_BYTES, &maps.b0, col + C::CH, kc, ti.e);
+            } else {
+              load3(sB, &maps.b0, ti.n0 + crank * C::CH, kc, ti.e);
+              load3(sB + C::CHUNK_BYTES, &maps.b1, ti.n0 + crank * C::CH, kc, ti.e);
+            }
           } else if constexpr (MODE == kFwdGateUp) {
             // K-major (transposed) weights: gate rows then up rows of the tile
             load3(sB, &maps.b0, kc, ti.n0, ti.e);
@@ -692,18 +710,34 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll 1
             for (int c = j0; c < j1; ++c) {
               float u[32];
-              int gcol, ucol;   // accumulator columns of this chunk's gate and up values
-              if constexpr (C::CTA2) {
-                static_assert(BN == 256, "gate_up pair tile layout");
-                const int tb = ti.half ? 0 : (c >> 1) * 128;
-                gcol = tb + (c & 1) * 32;
-                ucol = gcol + 64;
+              if constexpr (C::CTA2 && C::IL) {
+                // 64 accumulator columns of gate/up pairs: gate at even, up
+                // at odd columns
+                const int pb = (ti.half ? 0 : (c >> 1) * 128) + (c & 1) * 64;
+                float p0[32], p1[32];
+                tmem_ld32(tacc + pb, p0);
+                tmem_ld32(tacc + pb + 32, p1);
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                  v[i] = p0[2 * i];
+                  u[i] = p0[2 * i + 1];
+                  v[16 + i] = p1[2 * i];
+                  u[16 + i] = p1[2 * i + 1];
+                }
               } else {
-                gcol = c * 32;
-                ucol = BN / 2 + c * 32;
+                int gcol, ucol;   // accumulator columns of this chunk's gate and up values
+                if constexpr (C::CTA2) {
+                  static_assert(BN == 256, "gate_up pair tile layout");
+                  const int tb = ti.half ? 0 : (c >> 1) * 128;
+                  gcol = tb + (c & 1) * 32;
+                  ucol = gcol + 64;
+                } else {
+                  gcol = c * 32;
+                  ucol = BN / 2 + c * 32;
+                }
+                tmem_ld32(tacc + gcol, v);
+                tmem_ld32(tacc + ucol, u);
               }
-              tmem_ld32(tacc + gcol, v);
-              tmem_ld32(tacc + ucol, u);
               if (args.save_h1) {
                 store_tile<float>(args.out[1], 0, orow, ti.n0 + c * 32, v, my_epi, lane);
                 store_tile<float>(args.out[2], 0, orow, ti.n0 + c * 32, u, my_epi, lane);
@@ -803,9 +837,47 @@ __global__ void __launch_bounds__(192, 1)
                   du[i] = round_tf32(du[i]);
                   aw[i] = round_tf32(aw[i]);
                 }
-                store_tile<T>(args.out[0], 0, orow, i0, dg, my_epi, lane);
-                store_tile<T>(args.out[1], 0, orow, i0, du, my_epi, lane);
+                if constexpr (C::IL) {
+                  // dgate / dup of output i are columns 2i, 2i + 1 of dH1
+#pragma unroll
+                  for (int hh = 0; hh < 2; ++hh) {
+                    float t[32];
+#pragma unroll
+                    for (int p = 0; p < 16; ++p) {
+                      t[2 * p] = dg[16 * hh + p];
+                      t[2 * p + 1] = du[16 * hh + p];
+                    }
+                    store_tile<T>(args.out[0], 0, orow, 2 * i0 + 32 * hh, t, my_epi, lane);
+                  }
+                } else {
+                  store_tile<T>(args.out[0], 0, orow, i0, dg, my_epi, lane);
+                  store_tile<T>(args.out[1], 0, orow, i0, du, my_epi, lane);
+                }
                 store_tile<T>(args.out[2], 0, orow, i0, aw, my_epi, lane);
+              } else if constexpr (C::IL) {
+                // dgate / dup of output i are columns 2i, 2i + 1 of dH1: bf16
+                // hi parts, then the remainders, of 16 outputs at a time
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                  float t[32];
+#pragma unroll
+                  for (int p = 0; p < 16; ++p) {
+                    t[2 * p] = bf16_round(dg[16 * hh + p]);
+                    t[2 * p + 1] = bf16_round(du[16 * hh + p]);
+                  }
+                  store_tile<T>(args.out[0], 0, orow, 2 * i0 + 32 * hh, t, my_epi, lane);
+#pragma unroll
+                  for (int p = 0; p < 16; ++p) {
+                    t[2 * p] = dg[16 * hh + p] - bf16_round(dg[16 * hh + p]);
+                    t[2 * p + 1] = du[16 * hh + p] - bf16_round(du[16 * hh + p]);
+                  }
+                  store_tile<T>(args.out[3], 0, orow, 2 * i0 + 32 * hh, t, my_epi, lane);
+                }
+                float lo[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) split_bf16(aw[i], aw[i], lo[i]);
+                store_tile<T>(args.out[2], 0, orow, i0, aw, my_epi, lane);
+                store_tile<T>(args.out[5], 0, orow, i0, lo, my_epi, lane);
               } else {
                 // bf16 hi parts (operands of the dgrad and the wgrads) and lo
                 // parts (the remainders, operands of the wgrads only)
@@ -877,11 +949,11 @@ __global__ void __launch_bounds__(192, 1)
   }
 }
 
-template <typename T, int MODE, int BN, int STAGES>
+template <typename T, int MODE, int BN, int STAGES, bool IL = false>
 cudaError_t launch_gemm_t(const GemmMaps& maps, const GemmArgs& args, int num_sms,
                           cudaStream_t st) {
-  using C = GemmCfg<T, MODE, BN, STAGES>;
-  auto kern = moe_gemm_kernel<T, MODE, BN, STAGES>;
+  using C = GemmCfg<T, MODE, BN, STAGES, IL>;
+  auto kern = moe_gemm_kernel<T, MODE, BN, STAGES, IL>;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;

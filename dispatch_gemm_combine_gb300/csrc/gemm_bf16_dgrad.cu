@@ -8,7 +8,9 @@ cudaError_t launch_gemm_bf16_dgrad(int mode, const GemmMaps& maps, const GemmArg
                                    cudaStream_t st) {
   using T = __nv_bfloat16;
   switch (mode) {
-    case kDgradDown: return launch_gemm_t<T, kDgradDown, 256, 3>(maps, a, sms, st);
+    case kDgradDown:
+      return a.gu_interleaved ? launch_gemm_t<T, kDgradDown, 256, 3, true>(maps, a, sms, st)
+                              : launch_gemm_t<T, kDgradDown, 256, 3>(maps, a, sms, st);
     case kDgradGateUp: return launch_gemm_t<T, kDgradGateUp, 256, 6>(maps, a, sms, st);
     default: return cudaErrorInvalidValue;
   }

@@ -10,7 +10,9 @@ cudaError_t launch_gemm_f32(int mode, const GemmMaps& maps, const GemmArgs& a, i
   switch (mode) {
     case kFwdGateUp: return launch_gemm_t<T, kFwdGateUp, 256, 4>(maps, a, sms, st);
     case kFwdDown: return launch_gemm_t<T, kFwdDown, 256, 4>(maps, a, sms, st);
-    case kDgradDown: return launch_gemm_t<T, kDgradDown, 256, 3>(maps, a, sms, st);
+    case kDgradDown:   // (the TF32 gate_up forward reads either layout through strided views)
+      return a.gu_interleaved ? launch_gemm_t<T, kDgradDown, 256, 3, true>(maps, a, sms, st)
+                              : launch_gemm_t<T, kDgradDown, 256, 3>(maps, a, sms, st);
     case kDgradGateUp: return launch_gemm_t<T, kDgradGateUp, 256, 4>(maps, a, sms, st);
     case kWgradDown: return launch_gemm_t<T, kWgradDown, 256, 4>(maps, a, sms, st);
     case kWgradGateUp: return launch_gemm_t<T, kWgradGateUp, 256, 3>(maps, a, sms, st);

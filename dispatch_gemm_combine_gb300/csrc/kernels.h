@@ -80,6 +80,7 @@ struct GemmArgs {
   int m_tiles;          // weight-gradient modes: 128-row tiles of the output
   int num_kb;           // row-grouped modes: 128-byte k-blocks of the contraction
   int act;
+  int gu_interleaved;   // fused gate_up columns: 0 [gate | up], 1 gate/up interleaved
   float limit;
   float alpha;
   int save_h1;          // kFwdGateUp: also store the gate / up pre-activations

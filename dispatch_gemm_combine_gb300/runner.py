@@ -16,8 +16,8 @@ _TORCH_DTYPE = {MOE_BF16: torch.bfloat16, MOE_FP32: torch.float32}
 
 class LayerRunner:
     def __init__(self, T, H, I, E, k, act, dtype=MOE_BF16, clamp_limit=7.0, alpha=1.702,
-                 device="cuda", training=True, backward=True):
-        self.shape = Shape(T, H, I, E, k, act, dtype, clamp_limit, alpha)
+                 device="cuda", training=True, backward=True, gate_up_layout=0):
+        self.shape = Shape(T, H, I, E, k, act, dtype, clamp_limit, alpha, gate_up_layout)
         self.device = device
         self.tdtype = _TORCH_DTYPE[dtype]
         self.plan_t, self.plan_s = alloc_plan(self.shape, device)

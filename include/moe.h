@@ -67,6 +67,12 @@ typedef enum {
 
 typedef enum { MOE_ACT_SWIGLU = 0, MOE_ACT_CLAMPED_GLU = 1 } moe_act;
 typedef enum { MOE_BF16 = 0, MOE_FP32 = 1 } moe_dtype;
+/* Column layout of the fused gate_up weight w_gate_up[e] [H, 2I]: the
+ * pages name a fused gate_up projection without fixing its columns.
+ * CONCAT: gate = columns [0, I), up = [I, 2I).  INTERLEAVED: gate = the even
+ * columns, up = the odd ones (column 2i and 2i+1 belong to output i).
+ * dw_gate_up comes back in the same layout. */
+typedef enum { MOE_GATE_UP_CONCAT = 0, MOE_GATE_UP_INTERLEAVED = 1 } moe_gate_up_layout;
 
 /* Problem description (model dimensions named on the pages' workload lines:
  * hidden_size H, intermediate size I, number of experts E,
@@ -79,6 +85,7 @@ typedef struct {
   float clamp_limit;
   float alpha;
   int32_t dtype;        /* moe_dtype */
+  int32_t gate_up_layout;   /* moe_gate_up_layout */
 } moe_shape;
 
 /* Dispatch plan ("masked indexing" / "sparse token extraction" in the pages'
@@ -161,7 +168,7 @@ moe_status moe_ffn_fwd(const moe_shape* shape, const void* x,
  *   those with the saved context, which needs moe_saved_size() bytes of
  *   caller memory between the two calls instead.
  *   Outputs: dx [T,H]; d_topk_w [T,k] fp32; dw_gate_up [E,H,2I] fp32
- *   (d_gate = [:,:,:I], d_up = [:,:,I:]); dw_down [E,I,H] fp32.  Experts
+ *   (the gate and up columns as in the shape's gate_up_layout); dw_down [E,I,H] fp32.  Experts
  *   with no routed token get zero weight gradients.  All reductions run in
  *   a fixed order (no float atomics). */
 moe_status moe_ffn_bwd(const moe_shape* shape, const void* dy, const void* x,

@@ -99,6 +99,30 @@ def activation_grad(g, u, act, limit=CLAMP_LIMIT, alpha=CLAMP_ALPHA):
     raise ValueError("unknown activation %r" % (act,))
 
 
+def gate_up_concatenated(w_gate_up, layout):
+    """The fused gate_up weight [..., 2I] in the concatenated layout (gate =
+    columns [0, I), up = [I, 2I)), the layout every function here takes.
+    layout 0 is that layout already; layout 1 interleaves the two (gate =
+    the even columns, up = the odd ones).  The pages fix neither."""
+    w = _f64(w_gate_up)
+    if layout == 0:
+        return w
+    return np.concatenate([w[..., 0::2], w[..., 1::2]], axis=-1)
+
+
+def gate_up_in_layout(w_concat, layout):
+    """Inverse of gate_up_concatenated: a concatenated [..., 2I] array (a
+    weight or its gradient) in the given layout."""
+    w = _f64(w_concat)
+    if layout == 0:
+        return w
+    I = w.shape[-1] // 2
+    out = np.empty_like(w)
+    out[..., 0::2] = w[..., :I]
+    out[..., 1::2] = w[..., I:]
+    return out
+
+
 def route(logits, k):
     """Top-k routing of router logits [T, E] (the step before the layer).
 

@@ -181,3 +181,41 @@ def test_backward_recompute_is_bit_identical(act, dtype):
     run.check()
     for name, a, b in zip(("dx", "d_topk_w", "dw_gate_up", "dw_down"), saved, again):
         assert torch.equal(a, b), name
+
+
+@pytest.mark.parametrize("T,H,I,E,k,act,dtype,std", [
+    (600, 256, 200, 6, 4, ACT_CLAMPED_GLU, "bf16", 0.2),   # odd m-tiles (half units), N tail
+    (300, 136, 264, 5, 3, ACT_SWIGLU, "bf16", None),
+    (200, 128, 136, 5, 3, ACT_CLAMPED_GLU, "fp32", 0.2),
+])
+def test_interleaved_gate_up_parity(T, H, I, E, k, act, dtype, std):
+    """gate_up weights with interleaved gate/up columns: the layer equals the
+    oracle on the same weights taken apart into [gate | up], and dw_gate_up
+    comes back interleaved; the backward without a saved context too."""
+    from dispatch_gemm_combine_gb300 import MOE_BF16, MOE_FP32, MOE_GATE_UP_INTERLEAVED
+    from dispatch_gemm_combine_gb300.runner import LayerRunner
+    r = _recipe(T, H, I, E, k, act, seed=77 + T, dtype=dtype, std=std)
+    case = synth.make_case(r)
+    x, idx, w, wgu_il, wd, dy = oracle_inputs(case)       # the recipe's weights, read as interleaved
+    wgu = oracle.gate_up_concatenated(wgu_il, 1)
+    d = to_device(case)
+    run = LayerRunner(T, H, I, E, k, act, MOE_FP32 if dtype == "fp32" else MOE_BF16, r.limit,
+                      r.alpha, gate_up_layout=MOE_GATE_UP_INTERLEAVED)
+    run.plan(d.topk_idx)
+    y = run.forward(d.x, d.topk_idx, d.topk_w, d.w_gate_up, d.w_down)
+    grads = [t.clone() for t in run.backward(d.dy, d.x, d.topk_idx, d.topk_w, d.w_gate_up,
+                                             d.w_down)]
+    again = run.backward(d.dy, d.x, d.topk_idx, d.topk_w, d.w_gate_up, d.w_down, recompute=True)
+    torch.cuda.synchronize()
+    run.check()
+    assert_close("y", y.float().cpu().numpy(), oracle.moe_forward(x, idx, w, wgu, wd, act))
+    dx_ref, dw_ref, dwgu_ref, dwd_ref = oracle.moe_backward(dy, x, idx, w, wgu, wd, act)
+    dwgu_ref_il = oracle.gate_up_in_layout(dwgu_ref, 1)
+    dx, dtw, dwgu, dwd = grads
+    assert_close("dx", dx.float().cpu().numpy(), dx_ref)
+    assert_dw_close(dtw.cpu().numpy(), dw_ref)
+    assert_close("d_gate", dwgu[:, :, 0::2].cpu().numpy(), dwgu_ref_il[:, :, 0::2])
+    assert_close("d_up", dwgu[:, :, 1::2].cpu().numpy(), dwgu_ref_il[:, :, 1::2])
+    assert_close("d_down", dwd.cpu().numpy(), dwd_ref)
+    for name, a, b in zip(("dx", "d_topk_w", "dw_gate_up", "dw_down"), grads, again):
+        assert torch.equal(a, b), name

@@ -472,3 +472,14 @@ def test_route_special_cases():
     assert np.array_equal(i0, [[0], [0]]) and np.all(w0 == 1.0)
     counts, _, _, _ = oracle.dispatch_plan(i1, 12)      # routed ids feed the plan
     assert counts.sum() == 9 * 4
+
+
+def test_gate_up_layouts():
+    # interleaved [g0 u0 g1 u1 g2 u2] -> concatenated [g0 g1 g2 u0 u1 u2]
+    w = np.array([[10., 20., 11., 21., 12., 22.]])
+    assert np.array_equal(oracle.gate_up_concatenated(w, 1), [[10., 11., 12., 20., 21., 22.]])
+    assert np.array_equal(oracle.gate_up_concatenated(w, 0), w)
+    rng = np.random.default_rng(6)
+    c = rng.normal(size=(3, 5, 8))
+    assert np.array_equal(oracle.gate_up_concatenated(oracle.gate_up_in_layout(c, 1), 1), c)
+    assert np.array_equal(oracle.gate_up_in_layout(oracle.gate_up_concatenated(c, 1), 1), c)
