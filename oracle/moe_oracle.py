@@ -172,12 +172,14 @@ def dispatch_plan(topk_idx, E):
 
 
 def moe_forward(x, topk_idx, topk_w, w_gate_up, w_down, act,
-                limit=CLAMP_LIMIT, alpha=CLAMP_ALPHA, return_slots=False):
+                limit=CLAMP_LIMIT, alpha=CLAMP_ALPHA, return_slots=False,
+                b_gate_up=None, b_down=None):
     """Forward pass of the expert layer, in the token-repeat page's order.
 
     1. repeat each token k times: x_rep[s] = x[s // k]  (slot s = t*k + j);
-    2. for each expert e, pick its rows by masked indexing, h = x_rep @ Wgu[e],
-       a = act(h[:, :I], h[:, I:]), o = a @ Wd[e];
+    2. for each expert e, pick its rows by masked indexing, h = x_rep @ Wgu[e]
+       (+ b_gate_up[e]), a = act(h[:, :I], h[:, I:]), o = a @ Wd[e]
+       (+ b_down[e]);
     3. scale each slot's output by its routing weight;
     4. sum the k scaled outputs of each token.
 
@@ -201,8 +203,12 @@ def moe_forward(x, topk_idx, topk_w, w_gate_up, w_down, act,
         mask = flat == e
         I = np.shape(Wd[e])[0]
         h1 = x_rep[mask] @ _f64(Wgu[e])
+        if b_gate_up is not None:
+            h1 = h1 + _f64(b_gate_up[e])
         a = activation(h1[:, :I], h1[:, I:], act, limit, alpha)
         o[mask] = a @ _f64(Wd[e])
+        if b_down is not None:
+            o[mask] = o[mask] + _f64(b_down[e])
     y = (o * w[:, None]).reshape(T, k, H).sum(axis=1)
     if return_slots:
         return y, o
@@ -210,7 +216,8 @@ def moe_forward(x, topk_idx, topk_w, w_gate_up, w_down, act,
 
 
 def moe_backward(dy, x, topk_idx, topk_w, w_gate_up, w_down, act,
-                 limit=CLAMP_LIMIT, alpha=CLAMP_ALPHA, experts=None):
+                 limit=CLAMP_LIMIT, alpha=CLAMP_ALPHA, experts=None,
+                 b_gate_up=None, b_down=None):
     """Exact gradients of L = <dy, y> for the layer (backward page).
 
     Per expert e, over its rows (slots s with idx[s] == e, in slot order):
@@ -224,7 +231,12 @@ def moe_backward(dy, x, topk_idx, topk_w, w_gate_up, w_down, act,
       dx_t       += dh_s Wgu[e]^T                      (summed over the k slots of t)
     Experts with no rows get zero weight gradients.
 
-    Returns (dx [T,H], d_topk_w [T,k], dWgu [E,H,2I], dWd [E,I,H]) in float64.
+    With per-expert biases (h = x_s Wgu[e] + b_gate_up[e], o_s = a Wd[e] +
+    b_down[e]) the same formulas hold with these h and o, and the biases'
+    gradients are db_gate_up[e] = sum_s dh_s and db_down[e] = sum_s do_s.
+
+    Returns (dx [T,H], d_topk_w [T,k], dWgu [E,H,2I], dWd [E,I,H]) in float64,
+    and, when either bias is given, also (db_gate_up [E,2I], db_down [E,H]).
     With `experts` (an iterable of expert ids) only those experts' weight
     gradients are formed and the returned dWgu / dWd are dicts keyed by id;
     dx and d_topk_w are then complete only for tokens whose experts are all
@@ -247,6 +259,9 @@ def moe_backward(dy, x, topk_idx, topk_w, w_gate_up, w_down, act,
     I = np.shape(w_down[ids[0]])[0] if ids else 0
     dWgu = {} if subset else np.zeros((E, H, 2 * I), dtype=np.float64)
     dWd = {} if subset else np.zeros((E, I, H), dtype=np.float64)
+    with_bias = b_gate_up is not None or b_down is not None
+    dbgu = np.zeros((E, 2 * I), dtype=np.float64)
+    dbd = np.zeros((E, H), dtype=np.float64)
     for e in ids:
         rows = np.nonzero(flat == e)[0]
         Wg = _f64(w_gate_up[e])
@@ -260,9 +275,13 @@ def moe_backward(dy, x, topk_idx, topk_w, w_gate_up, w_down, act,
         dye = dy_rep[rows]
         we = w[rows]
         h1 = xe @ Wg
+        if b_gate_up is not None:
+            h1 = h1 + _f64(b_gate_up[e])
         g, u = h1[:, :I], h1[:, I:]
         a = activation(g, u, act, limit, alpha)
         o = a @ Wde
+        if b_down is not None:
+            o = o + _f64(b_down[e])
         d_w[rows] = np.sum(dye * o, axis=1)
         do = we[:, None] * dye
         dWd[e] = a.T @ do
@@ -271,7 +290,11 @@ def moe_backward(dy, x, topk_idx, topk_w, w_gate_up, w_down, act,
         dh = np.concatenate([da * dadg, da * dadu], axis=1)
         dWgu[e] = xe.T @ dh
         dx_rep[rows] = dh @ Wg.T
+        dbgu[e] = dh.sum(axis=0)
+        dbd[e] = do.sum(axis=0)
     dx = dx_rep.reshape(T, k, H).sum(axis=1)
+    if with_bias:
+        return dx, d_w.reshape(T, k), dWgu, dWd, dbgu, dbd
     return dx, d_w.reshape(T, k), dWgu, dWd
 
 

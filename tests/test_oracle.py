@@ -483,3 +483,30 @@ def test_gate_up_layouts():
     c = rng.normal(size=(3, 5, 8))
     assert np.array_equal(oracle.gate_up_concatenated(oracle.gate_up_in_layout(c, 1), 1), c)
     assert np.array_equal(oracle.gate_up_in_layout(oracle.gate_up_concatenated(c, 1), 1), c)
+
+
+def test_biases_finite_differences_and_identities():
+    """Per-expert biases: fp64 central differences for every gradient the
+    biases add or change, the exact identity <db_down, b_down> = <dy, y> -
+    <dy, y without b_down> (y is affine in b_down), and zero biases giving
+    the bias-free layer."""
+    x, idx, w, wgu, wd, dy = _rand_case(12, 16, 10, 4, 2, ACT_CLAMPED_GLU, seed=8)
+    rng = np.random.default_rng(9)
+    E, I, H = wd.shape
+    bgu = rng.normal(size=(E, 2 * I)) * 0.5
+    bd = rng.normal(size=(E, H)) * 0.5
+    act = ACT_CLAMPED_GLU
+    dx, dw, dwgu, dwd, dbgu, dbd = oracle.moe_backward(dy, x, idx, w, wgu, wd, act,
+                                                         b_gate_up=bgu, b_down=bd)
+    L = lambda: float(np.sum(dy * oracle.moe_forward(x, idx, w, wgu, wd, act,
+                                                      b_gate_up=bgu, b_down=bd)))
+    _fd_check(L, bgu, [(e, c) for e in range(E) for c in range(2 * I)], dbgu)
+    _fd_check(L, bd, [(e, c) for e in range(E) for c in range(H)], dbd)
+    _fd_check(L, w, [(t, j) for t in range(12) for j in range(2)], dw)
+    _fd_check(L, x, _random_coords(x.shape, 24, rng), dx)
+    _fd_check(L, wgu, _random_coords(wgu.shape, 24, rng), dwgu)
+    y_b = oracle.moe_forward(x, idx, w, wgu, wd, act, b_gate_up=bgu, b_down=bd)
+    y_nob = oracle.moe_forward(x, idx, w, wgu, wd, act, b_gate_up=bgu)
+    assert np.isclose(np.sum(dbd * bd), np.sum(dy * (y_b - y_nob)), rtol=1e-12)
+    y0 = oracle.moe_forward(x, idx, w, wgu, wd, act, b_gate_up=0 * bgu, b_down=0 * bd)
+    assert np.array_equal(y0, oracle.moe_forward(x, idx, w, wgu, wd, act))
