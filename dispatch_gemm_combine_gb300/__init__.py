@@ -16,11 +16,11 @@ import os
 
 __all__ = [
     "MOE_OK", "MOE_ACT_SWIGLU", "MOE_ACT_CLAMPED_GLU", "MOE_BF16", "MOE_FP32", "MoeShape",
-    "MoePlan", "MoeError", "lib", "library_path", "moe_workspace_size", "moe_saved_size",
+    "MoePlan", "MoeBias", "MoeError", "lib", "library_path", "moe_workspace_size", "moe_saved_size",
     "moe_plan", "moe_ffn_fwd", "moe_ffn_bwd", "moe_get_device_error", "moe_status_string",
     "moe_set_wait_timeout_ns", "moe_kernel_launch_count", "moe_profile_enable",
     "moe_profile_read", "moe_profile_kernel_name", "Shape", "alloc_plan", "workspace", "plan", "ffn_fwd", "ffn_bwd",
-    "check_device_error",
+    "bias_struct", "check_device_error",
 ]
 
 MOE_OK = 0
@@ -53,6 +53,12 @@ class MoePlan(ctypes.Structure):
                 ("perm", ctypes.c_void_p), ("inv", ctypes.c_void_p)]
 
 
+class MoeBias(ctypes.Structure):
+    """moe_bias_t: optional per-expert biases and their gradient outputs."""
+    _fields_ = [("b_gate_up", ctypes.c_void_p), ("b_down", ctypes.c_void_p),
+                ("db_gate_up", ctypes.c_void_p), ("db_down", ctypes.c_void_p)]
+
+
 class MoeError(RuntimeError):
     def __init__(self, status, where):
         self.status = status
@@ -82,9 +88,10 @@ def lib():
     L.moe_plan.restype = ctypes.c_int
     L.moe_route.argtypes = [S, P, P, P, PL, P, ctypes.c_size_t, P]
     L.moe_route.restype = ctypes.c_int
-    L.moe_ffn_fwd.argtypes = [S, P, P, P, P, P, PL, P, P, P, ctypes.c_size_t, P]
+    B = ctypes.POINTER(MoeBias)
+    L.moe_ffn_fwd.argtypes = [S, P, P, P, P, P, B, PL, P, P, P, ctypes.c_size_t, P]
     L.moe_ffn_fwd.restype = ctypes.c_int
-    L.moe_ffn_bwd.argtypes = [S, P, P, P, P, P, P, PL, P, P, P, P, P, P, ctypes.c_size_t, P]
+    L.moe_ffn_bwd.argtypes = [S, P, P, P, P, P, P, B, PL, P, P, P, P, P, P, ctypes.c_size_t, P]
     L.moe_ffn_bwd.restype = ctypes.c_int
     L.moe_get_device_error.argtypes = [P, P]
     L.moe_get_device_error.restype = ctypes.c_int
@@ -118,18 +125,21 @@ def moe_plan(shape, topk_idx, plan, ws, ws_bytes, stream):
     return lib().moe_plan(ctypes.byref(shape), topk_idx, ctypes.byref(plan), ws, ws_bytes, stream)
 
 
-def moe_ffn_fwd(shape, x, topk_idx, topk_w, w_gate_up, w_down, plan, y, saved, ws, ws_bytes,
-                stream):
+def _byref(st):
+    return ctypes.byref(st) if st is not None else None
+
+
+def moe_ffn_fwd(shape, x, topk_idx, topk_w, w_gate_up, w_down, bias, plan, y, saved, ws,
+                ws_bytes, stream):
     return lib().moe_ffn_fwd(ctypes.byref(shape), x, topk_idx, topk_w, w_gate_up, w_down,
-                             ctypes.byref(plan) if plan is not None else None, y, saved, ws,
-                             ws_bytes, stream)
+                             _byref(bias), _byref(plan), y, saved, ws, ws_bytes, stream)
 
 
-def moe_ffn_bwd(shape, dy, x, topk_idx, topk_w, w_gate_up, w_down, plan, saved, dx, d_topk_w,
-                dw_gate_up, dw_down, ws, ws_bytes, stream):
+def moe_ffn_bwd(shape, dy, x, topk_idx, topk_w, w_gate_up, w_down, bias, plan, saved, dx,
+                d_topk_w, dw_gate_up, dw_down, ws, ws_bytes, stream):
     return lib().moe_ffn_bwd(ctypes.byref(shape), dy, x, topk_idx, topk_w, w_gate_up, w_down,
-                             ctypes.byref(plan), saved, dx, d_topk_w, dw_gate_up, dw_down, ws,
-                             ws_bytes, stream)
+                             _byref(bias), _byref(plan), saved, dx, d_topk_w, dw_gate_up,
+                             dw_down, ws, ws_bytes, stream)
 
 
 def moe_get_device_error(ws, stream):
@@ -234,22 +244,32 @@ def route(shape, logits, topk_idx, topk_w, plan_struct=None, ws=None, stream=Non
            "moe_route")
 
 
+def bias_struct(b_gate_up=None, b_down=None, db_gate_up=None, db_down=None):
+    """MoeBias over torch tensors (None = absent), or None when all are absent."""
+    if all(t is None for t in (b_gate_up, b_down, db_gate_up, db_down)):
+        return None
+    return MoeBias(_ptr(b_gate_up), _ptr(b_down), _ptr(db_gate_up), _ptr(db_down))
+
+
 def plan(shape, topk_idx, plan_struct, ws, stream=None):
     _check(moe_plan(shape, _ptr(topk_idx), plan_struct, _ptr(ws), ws.numel(), _stream(stream)),
            "moe_plan")
 
 
 def ffn_fwd(shape, x, topk_idx, topk_w, w_gate_up, w_down, y, ws, plan_struct=None, saved=None,
-            stream=None):
+            stream=None, bias=None):
+    """bias: a MoeBias (see bias_struct) or None."""
     _check(moe_ffn_fwd(shape, _ptr(x), _ptr(topk_idx), _ptr(topk_w), _ptr(w_gate_up),
-                       _ptr(w_down), plan_struct, _ptr(y), _ptr(saved), _ptr(ws), ws.numel(),
-                       _stream(stream)), "moe_ffn_fwd")
+                       _ptr(w_down), bias, plan_struct, _ptr(y), _ptr(saved), _ptr(ws),
+                       ws.numel(), _stream(stream)), "moe_ffn_fwd")
 
 
 def ffn_bwd(shape, dy, x, topk_idx, topk_w, w_gate_up, w_down, plan_struct, saved, dx, d_topk_w,
-            dw_gate_up, dw_down, ws, stream=None):
+            dw_gate_up, dw_down, ws, stream=None, bias=None):
+    """bias: a MoeBias (see bias_struct; it also names the bias-gradient
+    outputs) or None."""
     _check(moe_ffn_bwd(shape, _ptr(dy), _ptr(x), _ptr(topk_idx), _ptr(topk_w), _ptr(w_gate_up),
-                       _ptr(w_down), plan_struct, _ptr(saved), _ptr(dx), _ptr(d_topk_w),
+                       _ptr(w_down), bias, plan_struct, _ptr(saved), _ptr(dx), _ptr(d_topk_w),
                        _ptr(dw_gate_up), _ptr(dw_down), _ptr(ws), ws.numel(), _stream(stream)),
            "moe_ffn_bwd")
 

@@ -73,12 +73,13 @@ std::atomic<uint64_t> g_timeout_ns{2000000000ull};
 // Kernel kinds, for the launch counter and the optional event timer.
 enum Kind : int {
   kKPlan = 0, kKOffsets, kKGather, kKFwdGateUp, kKFwdDown, kKCombine, kKDgradDown, kKDwReduce,
-  kKWgradDown, kKDgradGateUp, kKWgradGateUp, kKMemset, kKTranspose, kKRoute, kNumKinds
+  kKWgradDown, kKDgradGateUp, kKWgradGateUp, kKMemset, kKTranspose, kKRoute, kKBiasDot,
+  kKBiasGrad, kNumKinds
 };
 const char* const kKindNames[kNumKinds] = {
     "plan", "padded_offsets", "gather_rows", "gemm_fwd_gate_up_act", "gemm_fwd_down_scale",
     "combine", "gemm_dgrad_down_act_bwd", "dw_reduce", "gemm_wgrad_down", "gemm_dgrad_gate_up",
-    "gemm_wgrad_gate_up", "memset", "transpose_f32", "route"};
+    "gemm_wgrad_gate_up", "memset", "transpose_f32", "route", "bias_slot_dot", "bias_colsum"};
 
 std::atomic<uint64_t> g_launches{0};
 std::atomic<int> g_profile{0};
@@ -303,7 +304,8 @@ Layout layout(const moe_shape* s, int which) {
       L.wguR = take(sizeof(float) * s->E * 2ull * s->I * s->H);
     }
     L.dxp = take(sizeof(float) * R * s->H);
-    L.dwpart = take(sizeof(float) * R * dgrad_down_ntiles(s));
+    // one partial per 256-column tile of the down dgrad, then the b_down term
+    L.dwpart = take(sizeof(float) * R * (dgrad_down_ntiles(s) + 1));
   }
   if (which == 3) {   // backward without a saved context: recompute it
     L.xp = take(es * R * s->H);
@@ -315,6 +317,18 @@ Layout layout(const moe_shape* s, int which) {
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+// The optional biases with a NULL struct read as "all NULL"; every pointer
+// that is given must be 16-byte aligned.
+moe_bias_t bias_or_none(const moe_bias_t* b) {
+  moe_bias_t z;
+  std::memset(&z, 0, sizeof(z));
+  return b ? *b : z;
+}
+bool bias_aligned(const moe_bias_t& b) {
+  auto ok = [](const void* p) { return !p || aligned16(p); };
+  return ok(b.b_gate_up) && ok(b.b_down) && ok(b.db_gate_up) && ok(b.db_down);
+}
 
 template <typename P>
 P* at(void* ws, size_t off) {
@@ -348,10 +362,12 @@ GemmArgs base_args(const moe_shape* s, const int* poff, const int* counts, const
   return a;
 }
 
-// gate_up GEMM + activation on the grouped rows xp: the activation into
-// aact [R, I] and, when h1 is given, the fp32 pre-activations [R, 2I]
-// (gate | up).  fp32 storage first transposes the weights into wguT.
-moe_status enqueue_gate_up(const moe_shape* s, const void* xp, const void* w_gate_up, float* wguT,
+// gate_up GEMM (+ the optional bias b_gate_up) + activation on the grouped
+// rows xp: the activation into aact [R, I] and, when h1 is given, the fp32
+// pre-activations [R, 2I] (gate | up).  fp32 storage first transposes the
+// weights into wguT.
+moe_status enqueue_gate_up(const moe_shape* s, const void* xp, const void* w_gate_up,
+                           const void* b_gate_up, float* wguT,
                            void* aact, float* h1, int* poff, const int* counts,
                            const int* offsets, const int* perm, const float* topk_w, int* err,
                            int sms, cudaStream_t st) {
@@ -396,6 +412,7 @@ moe_status enqueue_gate_up(const moe_shape* s, const void* xp, const void* w_gat
   a1.num_kb = (H + BK - 1) / BK;
   a1.n_tiles = (I + gemm_block_n(kFwdGateUp, es) - 1) / gemm_block_n(kFwdGateUp, es);
   a1.save_h1 = h1 ? 1 : 0;
+  a1.bias = b_gate_up;
   MOE_CUDA(tracked(kKFwdGateUp, 1, st, [&] { return launch_gemm(kFwdGateUp, es, m1, a1, sms, st); }));
   return MOE_OK;
 }
@@ -512,9 +529,11 @@ moe_status moe_route(const moe_shape* s, const float* logits, int32_t* topk_idx,
 
 moe_status moe_ffn_fwd(const moe_shape* s, const void* x, const int32_t* topk_idx,
                        const float* topk_w, const void* w_gate_up, const void* w_down,
-                       const moe_plan_t* plan, void* y, void* saved, void* ws, size_t ws_bytes,
-                       moe_stream_t stream) {
+                       const moe_bias_t* bias_in, const moe_plan_t* plan, void* y, void* saved,
+                       void* ws, size_t ws_bytes, moe_stream_t stream) {
   if (!shape_ok(s) || !ws || !w_gate_up || !w_down) return MOE_ERR_INVALID_ARG;
+  const moe_bias_t bias = bias_or_none(bias_in);
+  if (!bias_aligned(bias)) return MOE_ERR_INVALID_ARG;
   if (s->T == 0) return MOE_OK;
   if (!x || !topk_idx || !topk_w || !y) return MOE_ERR_INVALID_ARG;
   if (plan && (!plan->counts || !plan->offsets || !plan->perm || !plan->inv))
@@ -566,9 +585,9 @@ moe_status moe_ffn_fwd(const moe_shape* s, const void* x, const int32_t* topk_id
                               R, xp, es, sms, st);
   }));
 
-  const moe_status gs = enqueue_gate_up(s, xp, w_gate_up, es == 4 ? at<float>(ws, L.wguT) : nullptr,
-                                        aact, h1_saved, poff, counts, offsets, perm, topk_w, err,
-                                        sms, st);
+  const moe_status gs = enqueue_gate_up(s, xp, w_gate_up, bias.b_gate_up,
+                                        es == 4 ? at<float>(ws, L.wguT) : nullptr, aact, h1_saved,
+                                        poff, counts, offsets, perm, topk_w, err, sms, st);
   if (gs != MOE_OK) return gs;
 
   const uint32_t BK = 128 / es, CH = 128 / es;
@@ -593,6 +612,7 @@ moe_status moe_ffn_fwd(const moe_shape* s, const void* x, const int32_t* topk_id
   m2.b1 = m2.b0;
   GemmArgs a2 = base_args(s, poff, counts, offsets, perm, topk_w, err);
   a2.out[0] = out_view(ow, H, R, H);
+  a2.bias = bias.b_down;
   a2.num_kb = (I + BK - 1) / BK;
   a2.n_tiles = (H + gemm_block_n(kFwdDown, es) - 1) / gemm_block_n(kFwdDown, es);
   MOE_CUDA(tracked(kKFwdDown, 1, st, [&] { return launch_gemm(kFwdDown, es, m2, a2, sms, st); }));
@@ -606,11 +626,13 @@ moe_status moe_ffn_fwd(const moe_shape* s, const void* x, const int32_t* topk_id
 
 moe_status moe_ffn_bwd(const moe_shape* s, const void* dy, const void* x, const int32_t* topk_idx,
                        const float* topk_w, const void* w_gate_up, const void* w_down,
-                       const moe_plan_t* plan, const void* saved, void* dx, float* d_topk_w,
-                       float* dw_gate_up, float* dw_down, void* ws, size_t ws_bytes,
-                       moe_stream_t stream) {
+                       const moe_bias_t* bias_in, const moe_plan_t* plan, const void* saved,
+                       void* dx, float* d_topk_w, float* dw_gate_up, float* dw_down, void* ws,
+                       size_t ws_bytes, moe_stream_t stream) {
   if (!shape_ok(s) || !ws || !w_gate_up || !w_down || !dw_gate_up || !dw_down)
     return MOE_ERR_INVALID_ARG;
+  const moe_bias_t bias = bias_or_none(bias_in);
+  if (!bias_aligned(bias)) return MOE_ERR_INVALID_ARG;
   int sms = 0;
   const moe_status ds = device_info(&sms);
   if (ds != MOE_OK) return ds;
@@ -623,6 +645,14 @@ moe_status moe_ffn_bwd(const moe_shape* s, const void* dy, const void* x, const 
       cudaError_t e2 = cudaMemsetAsync(dw_down, 0, sizeof(float) * E * static_cast<size_t>(I) * H, st);
       return e1 != cudaSuccess ? e1 : e2;
     }));
+    if (bias.db_gate_up)
+      MOE_CUDA(tracked(kKMemset, 1, st, [&] {
+        return cudaMemsetAsync(bias.db_gate_up, 0, sizeof(float) * E * 2ull * I, st);
+      }));
+    if (bias.db_down)
+      MOE_CUDA(tracked(kKMemset, 1, st, [&] {
+        return cudaMemsetAsync(bias.db_down, 0, sizeof(float) * E * static_cast<size_t>(H), st);
+      }));
     return MOE_OK;
   }
   if (!dy || !x || !topk_idx || !topk_w || !plan || !dx || !d_topk_w)
@@ -673,9 +703,9 @@ moe_status moe_ffn_bwd(const moe_shape* s, const void* dy, const void* x, const 
     // the activation output is not needed: it goes to the dH1 region, which
     // the down dgrad overwrites
     const moe_status gs =
-        enqueue_gate_up(s, xp, w_gate_up, es == 4 ? at<float>(ws, L.wguT) : nullptr, dh1,
-                        const_cast<float*>(h1_saved), poff, counts, offsets, perm, topk_w, err,
-                        sms, st);
+        enqueue_gate_up(s, xp, w_gate_up, bias.b_gate_up, es == 4 ? at<float>(ws, L.wguT) : nullptr,
+                        dh1, const_cast<float*>(h1_saved), poff, counts, offsets, perm, topk_w,
+                        err, sms, st);
     if (gs != MOE_OK) return gs;
   }
 
@@ -725,10 +755,30 @@ moe_status moe_ffn_bwd(const moe_shape* s, const void* dy, const void* x, const 
   a1.out[4] = out_view(static_cast<char*>(dh1lo) + up_off, 2ll * I, R, I);
   a1.out[5] = out_view(awlo, I, R, I);
   MOE_CUDA(tracked(kKDgradDown, 1, st, [&] { return launch_gemm(kDgradDown, es, m1, a1, sms, st); }));
+  // with a down bias, o = a Wd + b_down, so d(topk w) gains <dY, b_down>: one
+  // more partial row, summed last
+  if (bias.b_down)
+    MOE_CUDA(tracked(kKBiasDot, 1, st, [&] {
+      return launch_bias_slot_dot(dy, bias.b_down, H, s->k, E, topk_idx, inv, offsets, poff, Tk,
+                                  R, dwpart + static_cast<int64_t>(a1.n_tiles) * R, es, sms, st);
+    }));
   MOE_CUDA(tracked(kKDwReduce, 1, st, [&] {
-    return launch_dw_reduce(dwpart, a1.n_tiles, R, E, topk_idx, inv, offsets, poff, Tk, d_topk_w,
-                            st);
+    return launch_dw_reduce(dwpart, a1.n_tiles + (bias.b_down ? 1 : 0), R, E, topk_idx, inv,
+                            offsets, poff, Tk, d_topk_w, st);
   }));
+  // bias gradients: per-expert column sums of dH1 (hi + lo) and of w * dy
+  // (dy read in token order through the plan)
+  if (bias.db_gate_up)
+    MOE_CUDA(tracked(kKBiasGrad, 1, st, [&] {
+      return launch_expert_colsum(dh1, split ? dh1lo : nullptr, 2 * I, 2ll * I, 0, E, poff,
+                                  counts, offsets, perm, topk_w, static_cast<int>(Tk), false,
+                                  bias.db_gate_up, es, st);
+    }));
+  if (bias.db_down)
+    MOE_CUDA(tracked(kKBiasGrad, 1, st, [&] {
+      return launch_expert_colsum(dy, nullptr, H, H, s->k, E, poff, counts, offsets, perm,
+                                  topk_w, static_cast<int>(Tk), true, bias.db_down, es, st);
+    }));
 
   // (2) down wgrad: dWd[e] = (w*a)_e^T dYp_e  (w*a as a bf16 hi/lo pair)
   GemmMaps m2;

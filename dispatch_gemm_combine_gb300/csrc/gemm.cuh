@@ -330,6 +330,36 @@ __device__ __forceinline__ void split_bf16(float x, float& hi, float& lo) {
   lo = x - hi;
 }
 
+// Add the bias values p[0, N) of a column chunk to v: every lane of the warp
+// reads the same addresses (the chunk's columns are shared by the warp's
+// rows), so each 16-byte load is one broadcast.  Only p[0, n) exists (n a
+// multiple of 16 bytes' worth of elements); the rest belong to columns past
+// the output, which are not stored, and are left out.  p is 16-byte aligned.
+template <typename T, int N>
+__device__ __forceinline__ void add_bias(const T* p, int n, float (&v)[N]) {
+  constexpr int PER = 16 / static_cast<int>(sizeof(T));
+#pragma unroll
+  for (int j = 0; j < N / PER; ++j) {
+    if (j * PER < n) {
+      const uint4 q = __ldg(reinterpret_cast<const uint4*>(p) + j);
+      if constexpr (sizeof(T) == 2) {
+        const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&q);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float2 f = __bfloat1622float2(h[i]);
+          v[8 * j + 2 * i] += f.x;
+          v[8 * j + 2 * i + 1] += f.y;
+        }
+      } else {
+        v[4 * j] += __uint_as_float(q.x);
+        v[4 * j + 1] += __uint_as_float(q.y);
+        v[4 * j + 2] += __uint_as_float(q.z);
+        v[4 * j + 3] += __uint_as_float(q.w);
+      }
+    }
+  }
+}
+
 template <typename T, int MODE, int BN, int STAGES, bool IL>
 __global__ void __launch_bounds__(192, 1)
     moe_gemm_kernel(const __grid_constant__ GemmMaps maps, const __grid_constant__ GemmArgs args) {
@@ -738,6 +768,27 @@ __global__ void __launch_bounds__(192, 1)
                 tmem_ld32(tacc + gcol, v);
                 tmem_ld32(tacc + ucol, u);
               }
+              if (args.bias) {
+                // per-expert gate / up biases of this chunk's outputs
+                const int i0 = ti.n0 + c * 32;
+                const T* bg = static_cast<const T*>(args.bias) + static_cast<int64_t>(ti.e) * 2 * args.I;
+                // interleaved bias columns also when the weights are read
+                // through strided views (the fp32 path has no IL kernel)
+                if (C::IL || args.gu_interleaved) {
+                  float b[64];
+#pragma unroll
+                  for (int i = 0; i < 64; ++i) b[i] = 0.f;
+                  add_bias(bg + 2 * i0, 2 * (args.I - i0), b);
+#pragma unroll
+                  for (int i = 0; i < 32; ++i) {
+                    v[i] += b[2 * i];
+                    u[i] += b[2 * i + 1];
+                  }
+                } else {
+                  add_bias(bg + i0, args.I - i0, v);
+                  add_bias(bg + args.I + i0, args.I - i0, u);
+                }
+              }
               if (args.save_h1) {
                 store_tile<float>(args.out[1], 0, orow, ti.n0 + c * 32, v, my_epi, lane);
                 store_tile<float>(args.out[2], 0, orow, ti.n0 + c * 32, u, my_epi, lane);
@@ -766,6 +817,13 @@ __global__ void __launch_bounds__(192, 1)
             for (int c = c0; c < c1; ++c) {
               float w2[64];
               tmem_ld64(tacc + (c - (ti.half ? c0 : 0)) * 64, w2);
+              if (MODE == kFwdDown && args.bias) {
+                // the expert's down bias, before the routing weight
+                const int col = ti.n0 + c * 64;
+                add_bias(static_cast<const T*>(args.bias) +
+                             static_cast<int64_t>(ti.e) * args.out[0].cols + col,
+                         args.out[0].cols - col, w2);
+              }
 #pragma unroll
               for (int i = 0; i < 64; ++i) w2[i] *= scale;
               store_tile<float>(args.out[0], 0, orow, ti.n0 + c * 64,

@@ -48,6 +48,22 @@ cudaError_t launch_dw_reduce(const float* dwpart, int ntiles, int64_t rows_max, 
                              const int* inv, const int* offsets, const int* poff, int64_t Tk,
                              float* d_topk_w, cudaStream_t st);
 
+// ---- per-expert bias terms (permute.cu); elem_bytes 2 (bf16) or 4 (fp32)
+// out[row(s)] = <dy[s / k, :H], b_down[idx[s], :H]> for each slot s whose
+// padded row row(s) is valid, summed in fp32 in a fixed order.
+cudaError_t launch_bias_slot_dot(const void* dy, const void* b_down, int H, int k, int E,
+                                 const int* idx, const int* inv, const int* offsets,
+                                 const int* poff, int64_t Tk, int64_t rows_max, float* out,
+                                 int elem_bytes, int num_sms, cudaStream_t st);
+// out[e, c] = sum_{j < counts[e]} s_j * (src[r_j, c] (+ src2[r_j, c])) in fp32,
+// in a fixed order; r_j = poff[e] + j, or perm[offsets[e] + j] / gather_k when
+// gather_k > 0; s_j = topk_w[perm[offsets[e] + j]] when `weighted`, else 1.
+// src / src2 (optional) have row stride ld; C % 8 == 0.
+cudaError_t launch_expert_colsum(const void* src, const void* src2, int C, int64_t ld,
+                                 int gather_k, int E, const int* poff, const int* counts,
+                                 const int* offsets, const int* perm, const float* topk_w, int tk,
+                                 bool weighted, float* out, int elem_bytes, cudaStream_t st);
+
 // ---- grouped tensor-core GEMMs (gemm_*.cu)
 enum GemmMode : int {
   kFwdGateUp = 0,    // A_act = act(Xp Wgu[e]) (+ saved pre-activations)
@@ -84,6 +100,7 @@ struct GemmArgs {
   float limit;
   float alpha;
   int save_h1;          // kFwdGateUp: also store the gate / up pre-activations
+  const void* bias;     // kFwdGateUp: b_gate_up [E, 2I]; kFwdDown: b_down [E, H]; or null
   const void* h1;       // kDgradDown: saved pre-activations [rows_max, 2I]
   int I;
   float* dwpart;        // kDgradDown: [n_tiles][rows_max]

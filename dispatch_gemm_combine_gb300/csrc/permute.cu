@@ -6,8 +6,12 @@
 //             inputs are the fp32 rows the GEMM epilogues write)
 //   dw_reduce (fixed-order sum of the per-column-tile partial dot products
 //             that make d(topk weights))
-// All three are HBM-bound: one warp per row, 16-byte vector accesses,
-// grid sized as a multiple of the SM count.
+//   bias terms (the optional per-expert biases: the b_down term of
+//             d(topk weights) and the per-expert column sums that are the
+//             bias gradients)
+// All are HBM-bound and use 16-byte vector accesses.  The row kernels run one
+// warp per row on a grid sized as a multiple of the SM count; the column sums
+// run one thread per 8 columns of one expert.
 #include "kernels.h"
 
 namespace moe {
@@ -167,6 +171,134 @@ __global__ void __launch_bounds__(256) dw_reduce_kernel(const float* __restrict_
   d_topk_w[s] = acc;
 }
 
+__device__ __forceinline__ void load8(const __nv_bfloat16* p, float* a) {
+  const uint4 v = __ldg(reinterpret_cast<const uint4*>(p));
+  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 f = __bfloat1622float2(h[i]);
+    a[2 * i] = f.x;
+    a[2 * i + 1] = f.y;
+  }
+}
+__device__ __forceinline__ void load8(const float* p, float* a) {
+  const float4 x = __ldg(reinterpret_cast<const float4*>(p));
+  const float4 y = __ldg(reinterpret_cast<const float4*>(p) + 1);
+  a[0] = x.x; a[1] = x.y; a[2] = x.z; a[3] = x.w;
+  a[4] = y.x; a[5] = y.y; a[6] = y.z; a[7] = y.w;
+}
+
+// Bias term of d(topk weights): <dy[t], b_down[e]> for each slot s = t*k + j
+// routed to expert e, written at the slot's padded row.  One warp per slot;
+// it reads dy in token order (the k slots of a token run on neighbouring
+// warps, so a token's row comes from HBM once) and the bias row from L2.
+template <typename T>
+__global__ void __launch_bounds__(256) bias_slot_dot_kernel(
+    const T* __restrict__ dy, const T* __restrict__ bd, int H, int k, int E,
+    const int* __restrict__ idx, const int* __restrict__ inv, const int* __restrict__ offsets,
+    const int* __restrict__ poff, int64_t Tk, int64_t rows_max, float* __restrict__ out) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+  for (int64_t s = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+       s < Tk; s += warps) {
+    const int64_t p = padded_row_of_slot(static_cast<int>(s), E, idx, inv, offsets, poff);
+    if (p < 0 || p >= rows_max) continue;
+    const T* dr = dy + (s / k) * H;
+    const T* br = bd + static_cast<int64_t>(__ldg(idx + s)) * H;
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    int c = lane * 8;
+    for (; c + 3 * 256 < H; c += 4 * 256) {   // four 16-byte loads of each in flight
+      float a[4][8], b[4][8];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        load8(dr + c + u * 256, a[u]);
+        load8(br + c + u * 256, b[u]);
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[u] = fmaf(a[u][i], b[u][i], acc[u]);
+    }
+    for (; c < H; c += 256) {
+      float a[8], b[8];
+      load8(dr + c, a);
+      load8(br + c, b);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[0] = fmaf(a[i], b[i], acc[0]);
+    }
+    float v = (acc[0] + acc[1]) + (acc[2] + acc[3]);
+#pragma unroll
+    for (int d = 16; d > 0; d >>= 1) v += __shfl_xor_sync(0xffffffffu, v, d);
+    if (lane == 0) out[p] = v;
+  }
+}
+
+// Per-expert column sums over the expert's rows j = 0 .. counts[e]-1: the
+// bias gradients (dH1, its bf16 hi and lo parts added back together, for
+// b_gate_up; w * dy for b_down).  Row j is row poff[e] + j of src, or, with
+// gather_k > 0, token row perm[offsets[e] + j] / gather_k (dy in token order,
+// which stays in L2 while the expert rows are read).  A block takes 512
+// columns of one expert (blockIdx.y): 64 threads x 8 columns, and kRowGroups
+// groups of them take every kRowGroups-th row; the groups' sums are added in
+// group order at the end, so the result does not depend on timing.
+constexpr int kRowGroups = 4;
+
+template <typename T>
+__global__ void __launch_bounds__(64 * kRowGroups) expert_colsum_kernel(
+    const T* __restrict__ src, const T* __restrict__ src2, int C, int64_t ld, int gather_k,
+    const int* __restrict__ poff, const int* __restrict__ counts,
+    const int* __restrict__ offsets, const int* __restrict__ perm,
+    const float* __restrict__ topk_w, int tk, int weighted, float* __restrict__ out) {
+  __shared__ float4 part[kRowGroups][64][2];
+  const int e = blockIdx.y;
+  const int tx = threadIdx.x, g = threadIdx.y;
+  const int c = (blockIdx.x * 64 + tx) * 8;
+  float acc[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+  if (c < C) {
+    const int p0 = __ldg(poff + e);
+    const int n = min(__ldg(counts + e), __ldg(poff + e + 1) - p0);
+    const int g0 = __ldg(offsets + e);
+    const bool need_slot = gather_k > 0 || weighted;
+#pragma unroll 4
+    for (int j = g; j < n; j += kRowGroups) {
+      int slot = 0;
+      if (need_slot) {
+        const int gi = g0 + j;
+        slot = gi < tk ? __ldg(perm + gi) : -1;
+        if (slot < 0 || slot >= tk) continue;   // an inconsistent plan: contributes nothing
+      }
+      const int64_t r =
+          (gather_k > 0 ? static_cast<int64_t>(slot / gather_k) : static_cast<int64_t>(p0 + j)) *
+              ld + c;
+      float a[8];
+      load8(src + r, a);
+      if (src2) {
+        float b[8];
+        load8(src2 + r, b);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) a[i] += b[i];
+      }
+      const float sc = weighted ? __ldg(topk_w + slot) : 1.f;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[i] = fmaf(sc, a[i], acc[i]);
+    }
+  }
+  part[g][tx][0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+  part[g][tx][1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+  __syncthreads();
+  if (g == 0 && c < C) {
+#pragma unroll
+    for (int q = 1; q < kRowGroups; ++q) {
+      const float4 x = part[q][tx][0], y = part[q][tx][1];
+      acc[0] += x.x; acc[1] += x.y; acc[2] += x.z; acc[3] += x.w;
+      acc[4] += y.x; acc[5] += y.y; acc[6] += y.z; acc[7] += y.w;
+    }
+    store8(out + static_cast<int64_t>(e) * C + c, acc);
+  }
+}
+
 static int grid_for(int64_t rows, int num_sms) {
   // 8 warps per block; enough blocks to cover every SM several times.
   const int64_t need = (rows + 7) / 8;
@@ -237,6 +369,41 @@ cudaError_t launch_dw_reduce(const float* dwpart, int ntiles, int64_t rows_max, 
   const int blocks = static_cast<int>((Tk + 255) / 256);
   dw_reduce_kernel<<<blocks, 256, 0, st>>>(dwpart, ntiles, rows_max, E, idx, inv, offsets, poff,
                                            Tk, d_topk_w);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bias_slot_dot(const void* dy, const void* b_down, int H, int k, int E,
+                                 const int* idx, const int* inv, const int* offsets,
+                                 const int* poff, int64_t Tk, int64_t rows_max, float* out,
+                                 int elem_bytes, int num_sms, cudaStream_t st) {
+  if (Tk == 0) return cudaSuccess;
+  const int g = grid_for(Tk, num_sms);
+  if (elem_bytes == 2)
+    bias_slot_dot_kernel<<<g, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(dy),
+                                            static_cast<const __nv_bfloat16*>(b_down), H, k, E,
+                                            idx, inv, offsets, poff, Tk, rows_max, out);
+  else
+    bias_slot_dot_kernel<<<g, 256, 0, st>>>(static_cast<const float*>(dy),
+                                            static_cast<const float*>(b_down), H, k, E, idx, inv,
+                                            offsets, poff, Tk, rows_max, out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_expert_colsum(const void* src, const void* src2, int C, int64_t ld,
+                                 int gather_k, int E, const int* poff, const int* counts,
+                                 const int* offsets, const int* perm, const float* topk_w, int tk,
+                                 bool weighted, float* out, int elem_bytes, cudaStream_t st) {
+  if (C % 8 || E <= 0 || E > 65535) return cudaErrorInvalidValue;
+  const dim3 grid((C / 8 + 63) / 64, E), block(64, kRowGroups);
+  if (elem_bytes == 2)
+    expert_colsum_kernel<<<grid, block, 0, st>>>(
+        static_cast<const __nv_bfloat16*>(src), static_cast<const __nv_bfloat16*>(src2), C, ld,
+        gather_k, poff, counts, offsets, perm, topk_w, tk, weighted ? 1 : 0, out);
+  else
+    expert_colsum_kernel<<<grid, block, 0, st>>>(static_cast<const float*>(src),
+                                                 static_cast<const float*>(src2), C, ld, gather_k,
+                                                 poff, counts, offsets, perm, topk_w, tk,
+                                                 weighted ? 1 : 0, out);
   return cudaGetLastError();
 }
 

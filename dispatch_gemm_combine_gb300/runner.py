@@ -8,8 +8,8 @@ library's kernels.
 
 import torch
 
-from . import (MOE_BF16, MOE_FP32, Shape, alloc_plan, check_device_error, ffn_bwd, ffn_fwd,
-               moe_saved_size, plan, route, workspace)
+from . import (MOE_BF16, MOE_FP32, Shape, alloc_plan, bias_struct, check_device_error, ffn_bwd,
+               ffn_fwd, moe_saved_size, plan, route, workspace)
 
 _TORCH_DTYPE = {MOE_BF16: torch.bfloat16, MOE_FP32: torch.float32}
 
@@ -41,29 +41,42 @@ class LayerRunner:
         [T,E] and build the plan of the chosen ids."""
         route(self.shape, logits, topk_idx, topk_w, self.plan_s, self.ws_plan, stream)
 
-    def forward(self, x, topk_idx, topk_w, w_gate_up, w_down, use_plan=True, stream=None):
+    def forward(self, x, topk_idx, topk_w, w_gate_up, w_down, use_plan=True, stream=None,
+                b_gate_up=None, b_down=None):
         """y = layer(x).  With use_plan the plan must have been built by plan();
-        otherwise the forward builds its own inside the workspace."""
+        otherwise the forward builds its own inside the workspace.  b_gate_up
+        [E,2I] / b_down [E,H] (storage dtype) are the optional per-expert biases."""
         ffn_fwd(self.shape, x, topk_idx, topk_w, w_gate_up, w_down, self.y, self.ws_fwd,
-                self.plan_s if use_plan else None, self.saved, stream)
+                self.plan_s if use_plan else None, self.saved, stream,
+                bias_struct(b_gate_up, b_down))
         return self.y
 
-    def backward(self, dy, x, topk_idx, topk_w, w_gate_up, w_down, stream=None, recompute=False):
-        """Gradients of <dy, y>.  With recompute the saved context is not used:
-        the backward recomputes it in a larger workspace (allocated on first use)."""
+    def backward(self, dy, x, topk_idx, topk_w, w_gate_up, w_down, stream=None, recompute=False,
+                 b_gate_up=None, b_down=None):
+        """Gradients of <dy, y>: (dx, d_topk_w, dw_gate_up, dw_down), and with
+        biases also (db_gate_up, db_down).  The biases must be those given to
+        the forward.  With recompute the saved context is not used: the
+        backward recomputes it in a larger workspace (allocated on first use)."""
+        with_bias = b_gate_up is not None or b_down is not None
+        bias = None
+        if with_bias:
+            if getattr(self, "db_gate_up", None) is None:
+                E, H, I = self.shape.E, self.shape.H, self.shape.I
+                self.db_gate_up = torch.empty((E, 2 * I), dtype=torch.float32, device=self.device)
+                self.db_down = torch.empty((E, H), dtype=torch.float32, device=self.device)
+            bias = bias_struct(b_gate_up, b_down, self.db_gate_up, self.db_down)
         if recompute:
             if getattr(self, "ws_bwd_recompute", None) is None:
                 self.ws_bwd_recompute = workspace(self.shape, 3, self.device)
-            ffn_bwd(self.shape, dy, x, topk_idx, topk_w, w_gate_up, w_down, self.plan_s, None,
-                    self.dx, self.d_topk_w, self.dw_gate_up, self.dw_down, self.ws_bwd_recompute,
-                    stream)
+            ws, saved = self.ws_bwd_recompute, None
         else:
-            ffn_bwd(self.shape, dy, x, topk_idx, topk_w, w_gate_up, w_down, self.plan_s,
-                    self.saved, self.dx, self.d_topk_w, self.dw_gate_up, self.dw_down,
-                    self.ws_bwd, stream)
-        return self.dx, self.d_topk_w, self.dw_gate_up, self.dw_down
+            ws, saved = self.ws_bwd, self.saved
+        ffn_bwd(self.shape, dy, x, topk_idx, topk_w, w_gate_up, w_down, self.plan_s, saved,
+                self.dx, self.d_topk_w, self.dw_gate_up, self.dw_down, ws, stream, bias)
+        out = (self.dx, self.d_topk_w, self.dw_gate_up, self.dw_down)
+        return out + (self.db_gate_up, self.db_down) if with_bias else out
 
     def check(self, stream=None):
-        for ws in (self.ws_plan, self.ws_fwd, self.ws_bwd):
+        for ws in (self.ws_plan, self.ws_fwd, self.ws_bwd, getattr(self, "ws_bwd_recompute", None)):
             if ws is not None:
                 check_device_error(ws, stream)

@@ -104,6 +104,29 @@ typedef struct {
   int32_t* inv;
 } moe_plan_t;
 
+/* Optional per-expert biases.  The pages' layer has none; this variant of
+ * the layer adds one bias row per expert to each projection:
+ *   h = x Wgu[e] + b_gate_up[e],   o = act(h) Wd[e] + b_down[e],
+ *   y[t] = sum_j w[t,j] * o,
+ * so d(topk weights) also sees the bias (d_w = <dy, o>) and the gradients of
+ * the biases are db_gate_up[e] = sum, over the expert's rows, of dh (the
+ * gradient of h) and db_down[e] = sum of w * dy.
+ *   b_gate_up  [E,2I] storage dtype, columns in the shape's gate_up_layout
+ *   b_down     [E,H]  storage dtype
+ *   db_gate_up [E,2I] fp32, written by moe_ffn_bwd when non-NULL (same layout)
+ *   db_down    [E,H]  fp32, written by moe_ffn_bwd when non-NULL
+ * Every pointer may be NULL: a NULL bias is no bias (zero), a NULL gradient
+ * is not computed (a frozen bias).  A NULL moe_bias_t* means all four NULL.
+ * The backward must see the biases the forward used (the saved context
+ * holds h with b_gate_up added; b_down enters d(topk weights)).  Experts with
+ * no routed token get zero bias gradients; the sums run in a fixed row order. */
+typedef struct {
+  const void* b_gate_up;
+  const void* b_down;
+  float* db_gate_up;
+  float* db_down;
+} moe_bias_t;
+
 /* Bytes of workspace needed by one call: which = 0 moe_plan (and
  * moe_route with a plan), 1 moe_ffn_fwd, 2 moe_ffn_bwd with a saved
  * context, 3 moe_ffn_bwd without one (it then recomputes the context).
@@ -146,6 +169,8 @@ moe_status moe_route(const moe_shape* shape, const float* logits, int32_t* topk_
  * routing-weight scale -> deterministic k-way combine).
  *   x [T,H], topk_idx [T,k] int32, topk_w [T,k] fp32, w_gate_up [E,H,2I],
  *   w_down [E,I,H]  -> y [T,H].
+ *   bias: NULL, or the optional per-expert biases (moe_bias_t above; the
+ *         forward reads b_gate_up and b_down only).
  *   plan: a plan built by moe_plan for this topk_idx, or NULL to build one
  *         inside the workspace.
  *   saved: NULL (inference) or a buffer of moe_saved_size() bytes that
@@ -155,12 +180,14 @@ moe_status moe_route(const moe_shape* shape, const float* logits, int32_t* topk_
 moe_status moe_ffn_fwd(const moe_shape* shape, const void* x,
                        const int32_t* topk_idx, const float* topk_w,
                        const void* w_gate_up, const void* w_down,
+                       const moe_bias_t* bias,
                        const moe_plan_t* plan, void* y, void* saved,
                        void* ws, size_t ws_bytes, moe_stream_t stream);
 
 /* Backward pass of <dy, y>.
- *   dy [T,H]; x, topk_idx, topk_w, w_gate_up, w_down as given to the
- *   forward; plan: the plan of topk_idx (required).
+ *   dy [T,H]; x, topk_idx, topk_w, w_gate_up, w_down, bias as given to the
+ *   forward (bias also names the bias-gradient outputs); plan: the plan of
+ *   topk_idx (required).
  *   saved: the context the training forward wrote, or NULL.  With NULL the
  *   backward recomputes the context (the forward's gather of x and its
  *   gate_up GEMM, one third of the forward's FLOPs) into a workspace of
@@ -174,6 +201,7 @@ moe_status moe_ffn_fwd(const moe_shape* shape, const void* x,
 moe_status moe_ffn_bwd(const moe_shape* shape, const void* dy, const void* x,
                        const int32_t* topk_idx, const float* topk_w,
                        const void* w_gate_up, const void* w_down,
+                       const moe_bias_t* bias,
                        const moe_plan_t* plan, const void* saved,
                        void* dx, float* d_topk_w, float* dw_gate_up,
                        float* dw_down, void* ws, size_t ws_bytes,

@@ -166,6 +166,19 @@ def make_case(r: Recipe, device="cpu", with_dy=True, weight_chunk=8):
     return Case(r, x, ids, w, wgu, wd, dy)
 
 
+def make_biases(r: Recipe, device="cpu", std=0.5):
+    """Optional per-expert biases of recipe r: (b_gate_up [E, 2I], b_down
+    [E, H]) in the case dtype, N(0, std^2).  They come from their own
+    generator (seed r.seed + 1000003), so drawing them leaves make_case's
+    values unchanged.  b_gate_up's columns are in whatever layout the caller
+    reads the gate_up weight in."""
+    dt = _DTYPES[r.dtype]
+    g = _gen(r.seed + 1000003, device)
+    b_gate_up = _normal((r.E, 2 * r.I), std, g, device, dt)
+    b_down = _normal((r.E, r.H), std, g, device, dt)
+    return b_gate_up, b_down
+
+
 def routing_stats(topk_idx, E):
     """(fraction of experts with no token, max count / mean count)."""
     counts = torch.bincount(topk_idx.reshape(-1).long().cpu(), minlength=E).double()

@@ -70,12 +70,18 @@ def test_invalid_shapes(L, bad):
 def test_validation_before_device_access(L):
     s = L.Shape(16, 64, 64, 8, 2)
     # null workspace / pointers are rejected on the host
-    assert L.moe_ffn_fwd(s, 16, 16, 16, 16, 16, None, 16, None, None, 0, None) == L.MOE_ERR_INVALID_ARG
-    assert L.moe_ffn_fwd(s, 0, 16, 16, 16, 16, None, 16, None, 256, 1 << 30, None) == L.MOE_ERR_INVALID_ARG
+    assert L.moe_ffn_fwd(s, 16, 16, 16, 16, 16, None, None, 16, None, None, 0, None) == L.MOE_ERR_INVALID_ARG
+    assert L.moe_ffn_fwd(s, 0, 16, 16, 16, 16, None, None, 16, None, 256, 1 << 30, None) == L.MOE_ERR_INVALID_ARG
     # misaligned tensors
-    assert L.moe_ffn_fwd(s, 24, 16, 16, 16, 16, None, 16, None, 256, 1 << 30, None) == L.MOE_ERR_INVALID_ARG
+    assert L.moe_ffn_fwd(s, 24, 16, 16, 16, 16, None, None, 16, None, 256, 1 << 30, None) == L.MOE_ERR_INVALID_ARG
     # workspace too small
-    assert L.moe_ffn_fwd(s, 16, 16, 16, 16, 16, None, 16, None, 256, 8, None) == L.MOE_ERR_WORKSPACE
+    assert L.moe_ffn_fwd(s, 16, 16, 16, 16, 16, None, None, 16, None, 256, 8, None) == L.MOE_ERR_WORKSPACE
+    # a misaligned bias or bias gradient
+    for b in (L.MoeBias(24, None, None, None), L.MoeBias(None, 40, None, None)):
+        assert L.moe_ffn_fwd(s, 16, 16, 16, 16, 16, b, None, 16, None, 256, 1 << 30, None) == L.MOE_ERR_INVALID_ARG
+    b = L.MoeBias(None, None, 16, 8)
+    assert L.moe_ffn_bwd(s, 16, 16, 16, 16, 16, 16, b, L.MoePlan(16, 16, 16, 16), None, 16, 16, 16,
+                         16, 256, 1 << 30, None) == L.MOE_ERR_INVALID_ARG
     assert L.moe_status_string(L.MOE_ERR_BAD_INDEX) == "expert index out of range"
 
 
