@@ -37,18 +37,19 @@ class LazyExperts:
         return self.t[int(e)].cpu().double().numpy()
 
 
-def _run(r, backward):
+def _run(r, backward, biases=None):
     from dispatch_gemm_combine_gb300 import MOE_BF16
     from dispatch_gemm_combine_gb300.runner import LayerRunner
     case = synth.make_case(r, device="cuda", with_dy=backward)
     run = LayerRunner(r.T, r.H, r.I, r.E, r.k, r.act, MOE_BF16, r.limit, r.alpha,
                       training=backward, backward=backward)
+    bkw = {} if biases is None else dict(b_gate_up=biases[0], b_down=biases[1])
     run.plan(case.topk_idx)
-    y = run.forward(case.x, case.topk_idx, case.topk_w, case.w_gate_up, case.w_down)
+    y = run.forward(case.x, case.topk_idx, case.topk_w, case.w_gate_up, case.w_down, **bkw)
     grads = None
     if backward:
         grads = run.backward(case.dy, case.x, case.topk_idx, case.topk_w, case.w_gate_up,
-                             case.w_down)
+                             case.w_down, **bkw)
     torch.cuda.synchronize()
     run.check()
     return case, run, y, grads
@@ -148,3 +149,43 @@ def test_zipf_sweep(T):
     _check_tokens(case, y, grads, n_tok=6, seed=T)
     _check_expert_grads(case, run, grads, n_exp=1, seed=T + 1, max_rows=2048)
     _check_identities(case, y, grads)
+
+
+def test_clamped_glu_workload_with_biases():
+    """The bench step with per-expert biases on both projections: sampled
+    tokens and experts (their bias gradients included) against the oracle,
+    and, over every expert, y being linear in (Wd, b_down) jointly:
+    sum_e <dWd_e, Wd_e> + <db_down_e, b_down_e> = <dy, y>."""
+    r = synth.RECIPES["clamped_glu_fwd"]
+    bgu, bd = synth.make_biases(r, device="cuda")
+    case, run, y, grads = _run(r, backward=True, biases=(bgu, bd))
+    bgu_h, bd_h = bgu.double().cpu().numpy(), bd.double().cpu().numpy()
+    kw = dict(b_gate_up=bgu_h, b_down=bd_h)
+    g = np.random.default_rng(11)
+    toks = torch.from_numpy(np.sort(g.choice(r.T, size=16, replace=False)))
+    x, idx, w, dy = _host(case, toks)
+    wgu, wd = LazyExperts(case.w_gate_up), LazyExperts(case.w_down)
+    y_ref = oracle.moe_forward(x, idx, w, wgu, wd, r.act, r.limit, r.alpha, **kw)
+    assert_close("y[sample]", y[toks].double().cpu().numpy(), y_ref)
+    used = sorted(set(idx.reshape(-1).tolist()))
+    dx_ref, dw_ref = oracle.moe_backward(dy, x, idx, w, wgu, wd, r.act, r.limit, r.alpha,
+                                         experts=used, **kw)[:2]
+    assert_close("dx[sample]", grads[0][toks].double().cpu().numpy(), dx_ref)
+    assert_dw_close(grads[1][toks].cpu().numpy(), dw_ref)
+    for e in (int(v) for v in g.choice(r.E, size=2, replace=False)):
+        etoks = torch.nonzero((case.topk_idx == e).any(dim=1)).flatten().cpu()
+        x, idx, w, dy = _host(case, etoks)
+        _, _, dgu, dd, dbgu, dbd = oracle.moe_backward(dy, x, idx, w, wgu, wd, r.act, r.limit,
+                                                       r.alpha, experts=[e], **kw)
+        got_gu = grads[2][e].double().cpu().numpy()
+        assert_close("d_gate[%d]" % e, got_gu[:, :r.I], dgu[e][:, :r.I])
+        assert_close("d_up[%d]" % e, got_gu[:, r.I:], dgu[e][:, r.I:])
+        assert_close("d_down[%d]" % e, grads[3][e].double().cpu().numpy(), dd[e])
+        assert_close("db_gate_up[%d]" % e, grads[4][e].double().cpu().numpy(), dbgu[e])
+        assert_close("db_down[%d]" % e, grads[5][e].double().cpu().numpy(), dbd[e])
+    dyd, yd = case.dy.double(), y.double()
+    ly = float((dyd * yd).sum())
+    sw = float((case.topk_w.double() * grads[1].double()).sum())
+    sd = float((case.w_down.double() * grads[3].double()).sum() + (bd.double() * grads[5].double()).sum())
+    assert abs(sw - sd) <= 2e-3 * abs(sd), (sw, sd)
+    assert abs(sw - ly) <= 5e-3 * float(dyd.norm()) * float(yd.norm()), (sw, ly)
