@@ -5,7 +5,7 @@ import numpy as np
 import torch
 
 # Tolerances for bf16-input / fp32-accumulate outputs and gradients, and for
-# d(topk weights) (the spec parity rules of the layer).
+# d(topk weights): the parity bar of the layer, derived from its bf16 arithmetic.
 REL_FROB = 5e-3
 MAX_ABS_RMS = 3e-2
 DW_REL = 1e-2
