@@ -739,6 +739,9 @@ __global__ void __launch_bounds__(192, 1)
             const int j1 = ti.half ? j0 + 2 : BN / 64;
 #pragma unroll 1
             for (int c = j0; c < j1; ++c) {
+              // chunks past the last output column (the ragged last tile)
+              // have nothing to compute
+              if (ti.n0 + c * 32 >= args.I) break;
               float u[32];
               if constexpr (C::CTA2 && C::IL) {
                 // 64 accumulator columns of gate/up pairs: gate at even, up
@@ -815,6 +818,7 @@ __global__ void __launch_bounds__(192, 1)
             const int c1 = ti.half ? c0 + BN / 128 : BN / 64;
 #pragma unroll 1
             for (int c = c0; c < c1; ++c) {
+              if (ti.n0 + c * 64 >= args.out[0].cols) break;   // past the last output column
               float w2[64];
               tmem_ld64(tacc + (c - (ti.half ? c0 : 0)) * 64, w2);
               if (MODE == kFwdDown && args.bias) {
@@ -849,12 +853,14 @@ __global__ void __launch_bounds__(192, 1)
               }
               cp_async_commit();
             };
+            // column chunks that hold outputs (fewer in the ragged last tile)
+            const int nch = min(BN / 32, (args.I - ti.n0 + 31) / 32);
             prefetch(0);
             float dot = 0.f;
             auto run = [&](auto act_c) {
             constexpr int ACT = decltype(act_c)::value;
 #pragma unroll 1
-            for (int c = 0; c < BN / 32; ++c) {
+            for (int c = 0; c < nch; ++c) {
               tmem_ld32(tacc + c * 32, v);   // dA' (before the routing weight)
               const int i0 = ti.n0 + c * 32;
               float g[32], u[32];
@@ -869,7 +875,7 @@ __global__ void __launch_bounds__(192, 1)
               // refill the staging row with the next chunk as early as possible:
               // a use of every value read above orders those reads before the
               // copies that overwrite them
-              if (c + 1 < BN / 32) {
+              if (c + 1 < nch) {
                 float any = 0.f;
 #pragma unroll
                 for (int i = 0; i < 32; ++i) any += g[i] + u[i];
