@@ -63,3 +63,53 @@ def test_captured_step_replays_like_eager(act, dtype):
     run.check()
     for name, a, b in zip(("y", "dx", "d_topk_w", "dw_gate_up", "dw_down"), eager, _outputs(run)):
         assert torch.equal(a, b), name
+
+
+def test_captured_step_with_router_and_biases():
+    """The same for a step that starts from router logits (moe_route builds
+    the ids, weights and plan) and carries per-expert biases: every kernel
+    the step launches is captured and replayed bit for bit."""
+    from dispatch_gemm_combine_gb300 import MOE_BF16
+    from dispatch_gemm_combine_gb300.runner import LayerRunner
+    r = Recipe("graphb", T=500, H=256, I=200, E=12, k=3, act=ACT_CLAMPED_GLU, dtype="bf16",
+               weight_std=0.2, routing="softmax_topk_renorm", seed=21)
+    case = synth.make_case(r, device="cuda")
+    bgu, bd = synth.make_biases(r, device="cuda")
+    g = torch.Generator(device="cuda")
+    g.manual_seed(22)
+    logits = torch.randn((r.T, r.E), generator=g, device="cuda", dtype=torch.float32)
+    idx = torch.empty((r.T, r.k), dtype=torch.int32, device="cuda")
+    w = torch.empty((r.T, r.k), dtype=torch.float32, device="cuda")
+    run = LayerRunner(r.T, r.H, r.I, r.E, r.k, r.act, MOE_BF16, r.limit, r.alpha)
+    stream = torch.cuda.Stream()
+    outs = lambda: [t.clone() for t in (idx, w, run.y, run.dx, run.d_topk_w, run.dw_gate_up,
+                                        run.dw_down, run.db_gate_up, run.db_down)]
+
+    def step():
+        run.route(logits, idx, w)
+        run.forward(case.x, idx, w, case.w_gate_up, case.w_down, b_gate_up=bgu, b_down=bd)
+        run.backward(case.dy, case.x, idx, w, case.w_gate_up, case.w_down, b_gate_up=bgu,
+                     b_down=bd)
+
+    with torch.cuda.stream(stream):
+        step()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        step()
+    logits.copy_(torch.randn((r.T, r.E), generator=g, device="cuda", dtype=torch.float32))
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        step()
+    torch.cuda.synchronize()
+    eager = outs()
+    for t in (idx, run.y, run.dx, run.dw_gate_up, run.db_down):
+        t.fill_(-1)
+    with torch.cuda.stream(stream):
+        graph.replay()
+    torch.cuda.synchronize()
+    run.check()
+    names = ("topk_idx", "topk_w", "y", "dx", "d_topk_w", "dw_gate_up", "dw_down", "db_gate_up",
+             "db_down")
+    for name, a, b in zip(names, eager, outs()):
+        assert torch.equal(a, b), name
