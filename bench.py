@@ -268,6 +268,9 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="target length of the oracle sample (cpu_baseline)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--tokens", type=int, default=None,
+                    help="run the workload at this many tokens (the load-imbalance sweep's T "
+                         "values); the bench line itself uses the workload's own T")
     ap.add_argument("--experts", type=int, default=None,
                     help="profiling case: use this many experts and scale the tokens so each "
                          "expert keeps the workload's rows (not a bench line)")
@@ -294,6 +297,8 @@ def main():
     if world > 1:
         dist.init_process_group("nccl")
     r = synth.RECIPES[args.workload]
+    if args.tokens:
+        r = r.scaled(T=args.tokens)
     if args.experts:
         r = r.scaled(E=args.experts, T=max(1, r.T * args.experts // r.E))
     case = synth.make_case(r, device="cuda")
@@ -513,11 +518,11 @@ def main():
         "vs_baseline": None,
         "dtype": r.dtype,
         "data": "synthetic",
-        "config": {"workload": "%s fwd+bwd: T=%d H=%d I=%d E=%d top-%d clamped GLU (7.0, 1.702)"
-                   % (args.workload, r.T, r.H, r.I, r.E, r.k),
+        "config": {"workload": workload_name(args.workload, r),
                    "T": r.T, "H": r.H, "I": r.I, "E": r.E, "k": r.k, "seed": r.seed,
                    "parallelism": "replicas" if world > 1 else "single GPU",
-                   "l2": "no flush: 6.4 GB of expert weights per step exceed the 129 MB L2"},
+                   "l2": "no flush: %.1f GB of expert weights per step exceed the 129 MB L2"
+                         % (r.E * 3 * r.H * r.I * case.w_down.element_size() / 1e9)},
         "layer": {"fwd": layer_part(fwd_ms, f_fwd, b_fwd), "bwd": layer_part(bwd_ms, f_bwd, b_bwd),
                   "bwd_recompute_ms": round(bwd_re_ms, 4)},
         "roofline": roofline,
@@ -548,6 +553,11 @@ def main():
     return 0
 
 
+def workload_name(name, r):
+    act = "clamped GLU (%.1f, %g)" % (r.limit, r.alpha) if r.act == 1 else "SwiGLU"
+    return "%s fwd+bwd: T=%d H=%d I=%d E=%d top-%d %s" % (name, r.T, r.H, r.I, r.E, r.k, act)
+
+
 def run_reference(args, torch, synth):
     """Reference arm: the fp64 oracle on the host cores, each step a bounded
     token sample of the same workload (inputs drawn on the GPU when present,
@@ -569,8 +579,7 @@ def run_reference(args, torch, synth):
         "warmup": args.warmup, "ms_per_step": round(1e3 * t / args.steps, 2),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "impl": "reference",
-        "config": {"workload": "%s fwd+bwd: T=%d H=%d I=%d E=%d top-%d clamped GLU (7.0, 1.702)"
-                   % (args.workload, r.T, r.H, r.I, r.E, r.k), "sample_tokens": n_tok},
+        "config": {"workload": workload_name(args.workload, r), "sample_tokens": n_tok},
         "cpu_baseline": {"value": round(value, 5), "unit": "TFLOP/s", "cores": cpu_cores(),
                          "kind": "oracle", "sample": sample},
         "e2e": {"value": round(value, 5), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
