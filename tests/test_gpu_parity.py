@@ -219,3 +219,46 @@ def test_interleaved_gate_up_parity(T, H, I, E, k, act, dtype, std):
     assert_close("d_down", dwd.cpu().numpy(), dwd_ref)
     for name, a, b in zip(("dx", "d_topk_w", "dw_gate_up", "dw_down"), grads, again):
         assert torch.equal(a, b), name
+
+
+@pytest.mark.parametrize("T,H,I,E,k,act,dtype,layout,bias", [
+    (37, 8, 8, 3, 2, ACT_SWIGLU, "bf16", 0, False),           # one 16-byte row per token
+    (50, 16, 24, 1, 1, ACT_CLAMPED_GLU, "bf16", 1, True),     # a single expert
+    (65, 64, 8, 64, 32, ACT_SWIGLU, "bf16", 0, True),         # top-32, I of one row
+    (129, 8, 72, 5, 3, ACT_CLAMPED_GLU, "fp32", 1, True),     # fp32, H of one row
+    (300, 200, 8, 7, 7, ACT_SWIGLU, "fp32", 0, False),        # k = E: every expert per token
+])
+def test_extreme_shapes(T, H, I, E, k, act, dtype, layout, bias):
+    """The declared limits of the shape (H, I multiples of 8 from 8 up, any
+    T, 1 <= k <= E, one expert): boxes wider than the tensor, single-chunk
+    epilogues, every row of a tile padding but one."""
+    from dispatch_gemm_combine_gb300 import MOE_BF16, MOE_FP32
+    from dispatch_gemm_combine_gb300.runner import LayerRunner
+    r = _recipe(T, H, I, E, k, act, seed=900 + T, dtype=dtype, routing="uniform_ids", std=0.3)
+    case = synth.make_case(r)
+    x, idx, w, wgu_l, wd, dy = oracle_inputs(case)
+    wgu = oracle.gate_up_concatenated(wgu_l, layout)
+    kw, bkw = {}, {}
+    if bias:
+        bgu_t, bd_t = synth.make_biases(r)
+        kw = dict(b_gate_up=oracle.gate_up_concatenated(bgu_t.double().numpy(), layout),
+                  b_down=bd_t.double().numpy())
+        bkw = dict(b_gate_up=bgu_t.cuda(), b_down=bd_t.cuda())
+    d = to_device(case)
+    run = LayerRunner(T, H, I, E, k, act, MOE_FP32 if dtype == "fp32" else MOE_BF16, r.limit,
+                      r.alpha, gate_up_layout=layout)
+    run.plan(d.topk_idx)
+    y = run.forward(d.x, d.topk_idx, d.topk_w, d.w_gate_up, d.w_down, **bkw).clone()
+    grads = [t.clone() for t in run.backward(d.dy, d.x, d.topk_idx, d.topk_w, d.w_gate_up,
+                                             d.w_down, **bkw)]
+    torch.cuda.synchronize()
+    run.check()
+    assert_close("y", y.float().cpu().numpy(), oracle.moe_forward(x, idx, w, wgu, wd, act, **kw))
+    ref = oracle.moe_backward(dy, x, idx, w, wgu, wd, act, **kw)
+    assert_close("dx", grads[0].float().cpu().numpy(), ref[0])
+    assert_dw_close(grads[1].cpu().numpy(), ref[1])
+    assert_close("dw_gate_up", grads[2].cpu().numpy(), oracle.gate_up_in_layout(ref[2], layout))
+    assert_close("dw_down", grads[3].cpu().numpy(), ref[3])
+    if bias:
+        assert_close("db_gate_up", grads[4].cpu().numpy(), oracle.gate_up_in_layout(ref[4], layout))
+        assert_close("db_down", grads[5].cpu().numpy(), ref[5])
