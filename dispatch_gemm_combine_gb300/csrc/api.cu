@@ -608,7 +608,9 @@ moe_status moe_ffn_fwd(const moe_shape* s, const void* x, const int32_t* topk_id
     ok = ok && map3d(&m2.b0, es, wdT, I, H, E, I, static_cast<int64_t>(H) * I, BK, 256, SW);
   }
   if (!ok) return MOE_ERR_CUDA;
+  // bf16 tiles tokens on the MMA's N side; short units use a 32-row box
   m2.a2 = m2.a;
+  if (es == 2 && !map2d(&m2.a2, es, aact, I, R, I, BK, 32, SW)) return MOE_ERR_CUDA;
   m2.b1 = m2.b0;
   GemmArgs a2 = base_args(s, poff, counts, offsets, perm, topk_w, err);
   a2.out[0] = out_view(ow, H, R, H);
@@ -817,6 +819,7 @@ moe_status moe_ffn_bwd(const moe_shape* s, const void* dy, const void* x, const 
              dgrad_b_rows(kDgradGateUp, es), SW);
   if (!ok) return MOE_ERR_CUDA;
   m3.a2 = m3.a;
+  if (split && !map2d(&m3.a2, es, dh1, 2ll * I, R, 2ll * I, BK, 32, SW)) return MOE_ERR_CUDA;
   m3.b1 = m3.b0;
   GemmArgs a3 = base_args(s, poff, counts, offsets, perm, topk_w, err);
   a3.out[0] = out_view(dxp, H, R, H);

@@ -51,7 +51,7 @@ namespace moe {
 // that a CTA never exits with asynchronous work still writing its memory.
 constexpr uint64_t kDrainNs = 1000000000ull;
 
-template <typename T, int MODE, int BN, int STAGES, bool IL_ = false>
+template <typename T, int MODE, int BN, int STAGES, bool IL_ = false, bool SW_ = false>
 struct GemmCfg {
   static constexpr int kES = sizeof(T);
   static constexpr bool kTf32 = (kES == 4);
@@ -65,6 +65,14 @@ struct GemmCfg {
   // and the down dgrad), so the concatenated kernels are unchanged
   static constexpr bool IL = IL_;
   static_assert(!IL || MODE == kFwdGateUp || MODE == kDgradDown, "layout-specific modes only");
+  // Token-N tiling: the weights are the MMA's M operand (128 features per CTA,
+  // 256 per pair) and an expert's tokens its N side, in units of up to 256
+  // tokens rounded up to 16, so rows that only pad an expert to 128 cost no
+  // MMA work.  Used by the bf16 down projection and gate_up dgrad, whose
+  // epilogues write fp32 token rows.
+  static constexpr bool SW = SW_;
+  static_assert(!SW || (sizeof(T) == 2 && (MODE == kFwdDown || MODE == kDgradGateUp)),
+                "token-N tiling: bf16 down projection and gate_up dgrad");
   // 2-SM MMA over a CTA pair for every bf16 mode but the down dgrad, whose
   // heavy epilogue would hold up both CTAs (a pair's next MMA waits for both
   // CTAs' epilogues); TF32 keeps independent CTAs
@@ -73,8 +81,8 @@ struct GemmCfg {
   static constexpr int PAIR = CTA2 ? 2 : 1;
   // TF32 operands must be K-major (the fp32 path transposes the others into
   // the workspace first); 16-bit operands may be MN-major.
-  static constexpr bool A_MN = kWgrad && !kTf32;
-  static constexpr bool B_MN = (MODE == kFwdGateUp || MODE == kFwdDown || kWgrad) && !kTf32;
+  static constexpr bool A_MN = (kWgrad || (SW && MODE == kFwdDown)) && !kTf32;
+  static constexpr bool B_MN = !SW && (MODE == kFwdGateUp || MODE == kFwdDown || kWgrad) && !kTf32;
   // bf16 weight gradients contract a computed operand (w*a, dH1) that is
   // carried as a bf16 hi/lo pair: two MMAs, one per part, into the same
   // accumulator (about 16 bits of mantissa instead of 8).
@@ -129,6 +137,7 @@ struct TileInfo {
   int nt;      // column-tile index
   bool active; // false when this CTA's 128 rows lie past the expert (or the output)
   bool half;   // row-grouped pair unit of one 128-row tile (64 rows per CTA, M = 128)
+  int nn;      // token-N tiling: tokens (N) of this unit, a multiple of 16
 };
 
 // Work unit t of the schedule.  A unit is PAIR consecutive m-tiles with one
@@ -136,10 +145,11 @@ struct TileInfo {
 // 128 output rows for the weight gradients).  In row-grouped pairs, the
 // last unit of an expert with an odd number of m-tiles is a half unit: its
 // one m-tile is split into 64 rows per CTA.
-template <int BN_OUT, bool kWgrad, int PAIR>
+template <int BN_OUT, bool kWgrad, int PAIR, bool SW = false>
 __device__ __forceinline__ TileInfo decode_tile(const GemmArgs& a, int t, int bk, int rank) {
   TileInfo ti;
   ti.half = false;
+  ti.nn = 0;
   const int NT = a.n_tiles;
   if constexpr (kWgrad) {
     const int MP = (a.m_tiles + PAIR - 1) / PAIR;
@@ -176,6 +186,20 @@ __device__ __forceinline__ TileInfo decode_tile(const GemmArgs& a, int t, int bk
     const int local = t - (__ldg(up + lo) >> sh) * NT;
     ti.nt = local / mu;
     const int mp = local - ti.nt * mu;
+    if constexpr (SW) {
+      // token unit mp of the expert (mu = ceil(count / 256) of them): tokens
+      // [256 mp, min(count, 256 mp + 256)), N rounded up to 16; the pair's
+      // two CTAs hold its first and second N/2 token rows
+      const int left = __ldg(a.counts + lo) - mp * 256;
+      ti.nn = ((min(left, 256) + 15) >> 4) << 4;
+      ti.row0 = p0 + mp * 256;
+      ti.active = left > 0;
+      ti.m0 = 0;
+      ti.nkb = a.num_kb;
+      ti.klast = bk;
+      ti.n0 = ti.nt * BN_OUT;
+      return ti;
+    }
     const int m = mp * PAIR + rank;
     ti.active = m < mt;
     ti.row0 = p0 + m * 128;
@@ -278,6 +302,36 @@ __device__ __forceinline__ void store_tile(const OutDesc& o, int b, int r0, int 
   }
 }
 
+// Store a 32 x 32 fp32 tile held by columns (lane i holds column c0 + i of
+// rows r0 .. r0+31 in v[0..31]): the per-warp stage transposes it, then each
+// store writes whole 128-byte row segments, row r scaled by rs(r).  Rows >=
+// nrows and columns >= o.cols are not written.
+template <typename F>
+__device__ __forceinline__ void store_tile_t(const OutDesc& o, int r0, int c0,
+                                             const float (&v)[32], uint8_t* stage, int lane,
+                                             int nrows, F&& rs) {
+  float* base = static_cast<float*>(o.ptr);
+  float* st = reinterpret_cast<float*>(stage);
+#pragma unroll
+  for (int j = 0; j < 32; ++j) st[j * 36 + lane] = v[j];
+  __syncwarp();
+  const int c = (lane & 7) * 4;
+#pragma unroll
+  for (int it = 0; it < 8; ++it) {
+    const int r = it * 4 + (lane >> 3);
+    float4 val = *reinterpret_cast<const float4*>(st + r * 36 + c);
+    const float sc = rs(r);
+    val.x *= sc;
+    val.y *= sc;
+    val.z *= sc;
+    val.w *= sc;
+    const int gc = c0 + c;
+    if (r < nrows && gc < o.cols)
+      *reinterpret_cast<float4*>(base + static_cast<int64_t>(r0 + r) * o.ld + gc) = val;
+  }
+  __syncwarp();
+}
+
 // Store a 16-row x 64-column fp32 block read with tmem_ld16x64 straight from
 // registers: lane t writes 8 bytes at rows r0 + t/4 and r0 + 8 + t/4, so four
 // lanes fill one 32-byte sector.  Rows >= o.rows and columns >= o.cols (a
@@ -360,10 +414,10 @@ __device__ __forceinline__ void add_bias(const T* p, int n, float (&v)[N]) {
   }
 }
 
-template <typename T, int MODE, int BN, int STAGES, bool IL>
+template <typename T, int MODE, int BN, int STAGES, bool IL, bool SW>
 __global__ void __launch_bounds__(192, 1)
     moe_gemm_kernel(const __grid_constant__ GemmMaps maps, const __grid_constant__ GemmArgs args) {
-  using C = GemmCfg<T, MODE, BN, STAGES, IL>;
+  using C = GemmCfg<T, MODE, BN, STAGES, IL, SW>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t sbase = (raw + 1023u) & ~1023u;
@@ -444,7 +498,7 @@ __global__ void __launch_bounds__(192, 1)
     int64_t issued = 0;
     bool ok = true;
     for (int t = unit0; t < total && ok; t += ustride) {
-      const TileInfo ti = decode_tile<C::BN_OUT, C::kWgrad, C::PAIR>(args, t, C::BK, crank);
+      const TileInfo ti = decode_tile<C::BN_OUT, C::kWgrad, C::PAIR, C::SW>(args, t, C::BK, crank);
       for (int kb = 0; kb < ti.nkb; ++kb) {
         int good = 1;
         if (lane == 0) good = mbar_wait(empty_bar + 8 * stage, phase ^ 1u, tmo);
@@ -459,8 +513,12 @@ __global__ void __launch_bounds__(192, 1)
           const uint32_t fbt = leader_addr(fb);
           const uint32_t sA = s_stages + stage * C::STAGE_BYTES;
           const uint32_t sB = sA + C::A_BYTES;
+          // token-N tiling: a unit of at most 64 tokens (32 rows per CTA)
+          // loads its token rows with the 32-row box of maps.a2
+          const bool small_b = C::SW && ti.nn <= 64;
+          const uint32_t stage_tx = small_b ? C::A_BYTES + 32 * 128 : C::STAGE_BYTES;
           // the leader expects the bytes of both CTAs of the pair
-          if (leader) mbar_arrive_expect_tx(fb, C::PAIR * C::STAGE_BYTES);
+          if (leader) mbar_arrive_expect_tx(fb, C::PAIR * stage_tx);
           auto load2 = [&](uint32_t dst, const CUtensorMap* m, int c0, int c1) {
             if constexpr (C::CTA2)
               tma_load_2d_g2(dst, m, fbt, c0, c1);
@@ -474,6 +532,19 @@ __global__ void __launch_bounds__(192, 1)
               tma_load_3d(dst, m, fbt, c0, c1, c2);
           };
           const int kc = kb * C::BK;
+          if constexpr (C::SW) {
+            // A: this CTA's 128 features of the expert's weights (maps.b0);
+            // B: this CTA's half of the unit's token rows (maps.a)
+            const int f0 = ti.n0 + crank * 128;
+            if constexpr (C::A_MN) {
+#pragma unroll
+              for (int c = 0; c < 128 / C::CH; ++c)
+                load3(sA + c * C::CHUNK_BYTES, &maps.b0, f0 + c * C::CH, kc, ti.e);
+            } else {
+              load3(sA, &maps.b0, kc, f0, ti.e);
+            }
+            load2(sB, small_b ? &maps.a2 : &maps.a, kc, ti.row0 + crank * (ti.nn >> 1));
+          } else {
           // ---- A: this CTA's 128 rows
           if constexpr (C::kWgrad && !C::A_MN) {
             load2(sA, &maps.a, ti.row0 + kc, ti.m0);   // K-major (transposed) activations
@@ -527,6 +598,7 @@ __global__ void __launch_bounds__(192, 1)
                 load2(sB + part * C::B_PART + c * C::CHUNK_BYTES, part ? &maps.b1 : &maps.b0,
                       nb + c * C::CH, ti.row0 + kc);
           }
+          }
         }
         __syncwarp();
         ++issued;
@@ -555,7 +627,7 @@ __global__ void __launch_bounds__(192, 1)
       uint32_t acc_phase = 0;
       bool ok = true;
       for (int t = unit0; t < total && ok; t += ustride) {
-        const TileInfo ti = decode_tile<C::BN_OUT, C::kWgrad, C::PAIR>(args, t, C::BK, crank);
+        const TileInfo ti = decode_tile<C::BN_OUT, C::kWgrad, C::PAIR, C::SW>(args, t, C::BK, crank);
         int good = 1;
         if (lane == 0) good = mbar_wait(tempty_bar + 8 * acc, acc_phase ^ 1u, tmo);
         good = __shfl_sync(0xffffffffu, good, 0);
@@ -578,9 +650,12 @@ __global__ void __launch_bounds__(192, 1)
           if (lane == 0) {
             const uint32_t sA = s_stages + stage * C::STAGE_BYTES;
             const uint32_t sB = sA + C::A_BYTES;
+            const uint32_t idesc =
+                C::SW ? make_idesc(C::kTf32, C::A_MN, C::B_MN, 256, ti.nn)
+                      : (ti.half ? C::IDESC_HALF : C::IDESC);
             auto mma = [&](uint64_t ad, uint64_t bd, uint32_t accum) {
               if constexpr (C::CTA2)
-                tc_mma2(d_tmem, ad, bd, ti.half ? C::IDESC_HALF : C::IDESC, accum);
+                tc_mma2(d_tmem, ad, bd, idesc, accum);
               else
                 tc_mma<C::kTf32>(d_tmem, ad, bd, C::IDESC, accum);
             };
@@ -660,7 +735,7 @@ __global__ void __launch_bounds__(192, 1)
     };
 
     for (int t = unit0; t < total; t += ustride) {
-      const TileInfo ti = decode_tile<C::BN_OUT, C::kWgrad, C::PAIR>(args, t, C::BK, crank);
+      const TileInfo ti = decode_tile<C::BN_OUT, C::kWgrad, C::PAIR, C::SW>(args, t, C::BK, crank);
       int good = 1;
       if (lane == 0) good = mbar_wait(tfull_bar + 8 * acc, acc_phase, tmo);
       good = __shfl_sync(0xffffffffu, good, 0);
@@ -678,15 +753,56 @@ __global__ void __launch_bounds__(192, 1)
       // first tile row of this warp: a half unit's 64 rows per CTA are read
       // by quarters 0,1 (columns [0, N/2)) and again by 2,3 ([N/2, N))
       const int rq = ti.half ? (q & 1) * 32 : q * 32;
+      // token-N tiling: the warp's 32 features (output columns) must exist
       const bool warp_rows =
-          C::kWgrad || ti.row0 + rq - __ldg(args.poff + ti.e) < __ldg(args.counts + ti.e);
+          C::SW ? ti.n0 + crank * 128 + q * 32 < args.out[0].cols
+                : C::kWgrad || ti.row0 + rq - __ldg(args.poff + ti.e) < __ldg(args.counts + ti.e);
       if (ti.active && warp_rows) {
         const uint32_t tacc = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * C::ACC_COLS;
         const int row = ti.row0 + rq + lane;   // row-grouped modes: padded row of this thread
         const int orow = ti.row0 + rq;         // first row of this warp's output tiles
         float v[32];
 
-        if constexpr (C::kWgrad && !C::TMA_OUT) {
+        if constexpr (C::SW) {
+          // lane = feature (output column fcol + lane), accumulator column =
+          // token of the unit: each 32-token chunk is transposed into token
+          // rows; the down projection adds the bias and applies each token's
+          // routing weight
+          const int fcol = ti.n0 + crank * 128 + q * 32;
+          const int p0 = __ldg(args.poff + ti.e);
+          const int live = __ldg(args.counts + ti.e) - (ti.row0 - p0);   // tokens from row0
+          const int g0 = __ldg(args.offsets + ti.e) + (ti.row0 - p0);
+          float b = 0.f;
+          if (MODE == kFwdDown && args.bias && fcol + lane < args.out[0].cols)
+            b = to_f32(static_cast<const T*>(args.bias)[static_cast<int64_t>(ti.e) * args.out[0].cols + fcol + lane]);
+          // routing weight of token 32 c + lane, for every chunk c, loaded up
+          // front (independent loads); a row's weight then comes by shuffle
+          float wt[8];
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            const int tkn = c * 32 + lane;
+            float wv = 0.f;
+            if (MODE == kFwdDown && tkn < live && g0 + tkn < args.tk) {
+              const int slot = __ldg(args.perm + g0 + tkn);
+              if (slot >= 0 && slot < args.tk) wv = __ldg(args.topk_w + slot);
+            }
+            wt[c] = wv;
+          }
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            if (c * 32 >= ti.nn) break;   // warp-uniform
+            tmem_ld32(tacc + c * 32, v);
+            if (MODE == kFwdDown) {
+#pragma unroll
+              for (int j = 0; j < 32; ++j) v[j] += b;
+            }
+            const float wc = wt[c];
+            store_tile_t(args.out[0], ti.row0 + c * 32, fcol, v, my_epi, lane,
+                         min(32, live - c * 32), [&](int r) {
+                           return MODE == kFwdDown ? __shfl_sync(0xffffffffu, wc, r) : 1.f;
+                         });
+          }
+        } else if constexpr (C::kWgrad && !C::TMA_OUT) {
           // fp32 weight gradients go straight from tensor memory to global
           // memory in 16-row x 64-column blocks
 #pragma unroll 1
@@ -1013,11 +1129,11 @@ __global__ void __launch_bounds__(192, 1)
   }
 }
 
-template <typename T, int MODE, int BN, int STAGES, bool IL = false>
+template <typename T, int MODE, int BN, int STAGES, bool IL = false, bool SW = false>
 cudaError_t launch_gemm_t(const GemmMaps& maps, const GemmArgs& args, int num_sms,
                           cudaStream_t st) {
-  using C = GemmCfg<T, MODE, BN, STAGES, IL>;
-  auto kern = moe_gemm_kernel<T, MODE, BN, STAGES, IL>;
+  using C = GemmCfg<T, MODE, BN, STAGES, IL, SW>;
+  auto kern = moe_gemm_kernel<T, MODE, BN, STAGES, IL, SW>;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;

@@ -11,7 +11,7 @@ cudaError_t launch_gemm_bf16_dgrad(int mode, const GemmMaps& maps, const GemmArg
     case kDgradDown:
       return a.gu_interleaved ? launch_gemm_t<T, kDgradDown, 256, 3, true>(maps, a, sms, st)
                               : launch_gemm_t<T, kDgradDown, 256, 3>(maps, a, sms, st);
-    case kDgradGateUp: return launch_gemm_t<T, kDgradGateUp, 256, 6>(maps, a, sms, st);
+    case kDgradGateUp: return launch_gemm_t<T, kDgradGateUp, 256, 6, false, true>(maps, a, sms, st);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -112,7 +112,8 @@ struct GemmArgs {
 
 // TMA descriptors of the operands of one GEMM launch (unused ones may repeat
 // a valid map):
-//   a   A operand (hi part when split)      a2  A lo part (split A)
+//   a   A operand (hi part when split)      a2  A lo part (split A); with
+//       token-N tiling the token rows' 32-row box (a: 128 rows)
 //   b0  B operand (hi part / gate view)     b1  B lo part (split B) / up view
 //   out weight gradients: the fp32 dW [E, M, N], box {32, 32}, 128B swizzle
 struct GemmMaps {
