@@ -247,6 +247,36 @@ __device__ __forceinline__ void act_bwd(float g, float u, float L, float alpha, 
   }
 }
 
+// act_bwd for two elements at once on the packed fp32 pipe (two-wide fma,
+// add and mul; the comparisons, clamps and the exponential stay scalar).
+// The clamped GLU's ds/dg is written s (1 + alpha gc (1 - s)), the same
+// quantity as s + alpha gc s (1 - s).
+template <int ACT>
+__device__ __forceinline__ void act_bwd2(float2 g, float2 u, float L, float alpha, float2& a,
+                                         float2& dg, float2& du) {
+  const float2 one = make_float2(1.f, 1.f), mone = make_float2(-1.f, -1.f);
+  if constexpr (ACT == 0) {
+    const float2 s = make_float2(sigmoidf_(g.x), sigmoidf_(g.y));
+    const float2 sg = __fmul2_rn(g, s);
+    a = __fmul2_rn(sg, u);
+    const float2 oms = __ffma2_rn(s, mone, one);                    // 1 - s
+    dg = __fmul2_rn(__fmul2_rn(u, s), __ffma2_rn(g, oms, one));     // u s (1 + g (1 - s))
+    du = sg;
+  } else {
+    const float2 gc = make_float2(fminf(g.x, L), fminf(g.y, L));
+    const float2 uc = make_float2(fminf(fmaxf(u.x, -L), L), fminf(fmaxf(u.y, -L), L));
+    const float2 ag = __fmul2_rn(gc, make_float2(alpha, alpha));
+    const float2 s = make_float2(sigmoidf_(ag.x), sigmoidf_(ag.y));
+    const float2 glu = __fmul2_rn(gc, s);
+    const float2 up1 = __fadd2_rn(uc, one);
+    a = __fmul2_rn(up1, glu);
+    const float2 oms = __ffma2_rn(s, mone, one);
+    const float2 d = __fmul2_rn(up1, __fmul2_rn(s, __ffma2_rn(ag, oms, one)));
+    dg = make_float2(g.x <= L ? d.x : 0.f, g.y <= L ? d.y : 0.f);
+    du = make_float2((u.x >= -L && u.x <= L) ? glu.x : 0.f, (u.y >= -L && u.y <= L) ? glu.y : 0.f);
+  }
+}
+
 // Store this warp's 32x32 output tile: lane i holds row r0+i, columns
 // [c0, c0+32).  The tile goes through a per-warp shared-memory transpose
 // (rows padded so that both the row-wise writes and the column-wise reads
@@ -999,16 +1029,24 @@ __global__ void __launch_bounds__(192, 1)
                 prefetch(c + 1);
               }
               float dg[32], du[32], aw[32];
+              // two elements per step on the packed fp32 pipe; the dot
+              // product keeps an even and an odd partial sum
+              const float2 w2 = make_float2(wrow, wrow);
+              float2 dot2 = make_float2(0.f, 0.f);
 #pragma unroll
-              for (int i = 0; i < 32; ++i) {
-                float a, pg, pu;
-                act_bwd<ACT>(g[i], u[i], args.limit, args.alpha, a, pg, pu);
-                dot += v[i] * a;
-                const float da = wrow * v[i];
-                dg[i] = da * pg;
-                du[i] = da * pu;
-                aw[i] = wrow * a;
+              for (int i = 0; i < 32; i += 2) {
+                float2 a, pg, pu;
+                act_bwd2<ACT>(make_float2(g[i], g[i + 1]), make_float2(u[i], u[i + 1]),
+                              args.limit, args.alpha, a, pg, pu);
+                const float2 vv = make_float2(v[i], v[i + 1]);
+                dot2 = __ffma2_rn(vv, a, dot2);
+                const float2 da = __fmul2_rn(w2, vv);
+                const float2 rg = __fmul2_rn(da, pg), ru = __fmul2_rn(da, pu), ra = __fmul2_rn(w2, a);
+                dg[i] = rg.x; dg[i + 1] = rg.y;
+                du[i] = ru.x; du[i + 1] = ru.y;
+                aw[i] = ra.x; aw[i + 1] = ra.y;
               }
+              dot += dot2.x + dot2.y;
               if constexpr (C::kTf32) {
                 // operands of the TF32 dgrad / wgrad products
 #pragma unroll
