@@ -113,3 +113,43 @@ def test_captured_step_with_router_and_biases():
              "db_down")
     for name, a, b in zip(names, eager, outs()):
         assert torch.equal(a, b), name
+
+
+def test_two_streams_concurrently_match_alone():
+    """Two layers of different shapes, each with its own workspaces, enqueued
+    interleaved on two streams (their kernels may overlap on the GPU): every
+    output equals the same step run alone, bit for bit (the library keeps no
+    state that two calls with separate workspaces could share)."""
+    from dispatch_gemm_combine_gb300 import MOE_BF16
+    from dispatch_gemm_combine_gb300.runner import LayerRunner
+    recipes = [Recipe("s1", T=700, H=256, I=192, E=10, k=3, act=ACT_SWIGLU, dtype="bf16",
+                      weight_std="fan_in", routing="softmax_topk_renorm", seed=31),
+               Recipe("s2", T=400, H=384, I=320, E=6, k=2, act=ACT_CLAMPED_GLU, dtype="bf16",
+                      weight_std=0.2, routing="uniform_ids", seed=32)]
+    cases = [synth.make_case(r, device="cuda") for r in recipes]
+    runs = [LayerRunner(r.T, r.H, r.I, r.E, r.k, r.act, MOE_BF16, r.limit, r.alpha)
+            for r in recipes]
+
+    def step(run, c):
+        run.plan(c.topk_idx)
+        run.forward(c.x, c.topk_idx, c.topk_w, c.w_gate_up, c.w_down)
+        run.backward(c.dy, c.x, c.topk_idx, c.topk_w, c.w_gate_up, c.w_down)
+
+    def outs(run):
+        return [t.clone() for t in (run.y, run.dx, run.d_topk_w, run.dw_gate_up, run.dw_down)]
+
+    alone = []
+    for run, c in zip(runs, cases):
+        step(run, c)
+        torch.cuda.synchronize()
+        alone.append(outs(run))
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    for _ in range(3):
+        for run, c, st in zip(runs, cases, streams):
+            with torch.cuda.stream(st):
+                step(run, c)
+    torch.cuda.synchronize()
+    for run, ref in zip(runs, alone):
+        run.check()
+        for name, a, b in zip(("y", "dx", "d_topk_w", "dw_gate_up", "dw_down"), ref, outs(run)):
+            assert torch.equal(a, b), name
