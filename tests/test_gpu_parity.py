@@ -262,3 +262,45 @@ def test_extreme_shapes(T, H, I, E, k, act, dtype, layout, bias):
     if bias:
         assert_close("db_gate_up", grads[4].cpu().numpy(), oracle.gate_up_in_layout(ref[4], layout))
         assert_close("db_down", grads[5].cpu().numpy(), ref[5])
+
+
+@pytest.mark.parametrize("k", [1, 2])
+def test_expert_counts_at_tile_boundaries(k):
+    """Experts holding exactly 0, 1, 15-17, 64-65, 255-257, 271-273 and 511-513
+    rows: every edge of the 16-row token units, the 32-row warps, the
+    128-row tiles (half units) and the 256-row pairs, against the oracle."""
+    from dispatch_gemm_combine_gb300 import MOE_BF16
+    from dispatch_gemm_combine_gb300.runner import LayerRunner
+    counts = [1, 15, 16, 17, 255, 256, 257, 271, 272, 273, 511, 512, 513, 0, 64, 65]
+    E, H, I = len(counts), 128, 96
+    slots = np.repeat(np.arange(E), counts)               # each expert's rows, k per token
+    g = np.random.default_rng(41 + k)
+    slots = slots[g.permutation(slots.size)]
+    T = slots.size // k
+    idx = torch.from_numpy(slots[:T * k].reshape(T, k).astype(np.int32))
+    # fan-in weights: the structure is under test, not a heavy-tailed y (std 0.3 puts
+    # |y| at 8x its rms, where the bf16 output spacing alone exceeds 3e-2 rms)
+    r = _recipe(T, H, I, E, k, ACT_CLAMPED_GLU, seed=60 + k, routing="uniform_ids")
+    case = synth.make_case(r)
+    case.topk_idx = idx
+    x, idx_np, w, wgu, wd, dy = oracle_inputs(case)
+    d = to_device(case)
+    run = LayerRunner(T, H, I, E, k, r.act, MOE_BF16, r.limit, r.alpha)
+    run.plan(d.topk_idx)
+    y = run.forward(d.x, d.topk_idx, d.topk_w, d.w_gate_up, d.w_down).clone()
+    dx, dtw, dwgu, dwd = [t.clone() for t in run.backward(d.dy, d.x, d.topk_idx, d.topk_w,
+                                                          d.w_gate_up, d.w_down)]
+    torch.cuda.synchronize()
+    run.check()
+    got = np.bincount(idx_np.reshape(-1), minlength=E)
+    assert np.array_equal(run.plan_t["counts"].cpu().numpy(), got)
+    assert_close("y", y.float().cpu().numpy(), oracle.moe_forward(x, idx_np, w, wgu, wd, r.act))
+    ref = oracle.moe_backward(dy, x, idx_np, w, wgu, wd, r.act)
+    assert_close("dx", dx.float().cpu().numpy(), ref[0])
+    assert_dw_close(dtw.cpu().numpy(), ref[1])
+    for e in range(E):   # per expert: each boundary case on its own
+        if got[e]:
+            assert_close("dw_gate_up[%d]" % e, dwgu[e].cpu().numpy(), ref[2][e])
+            assert_close("dw_down[%d]" % e, dwd[e].cpu().numpy(), ref[3][e])
+        else:
+            assert torch.all(dwgu[e] == 0) and torch.all(dwd[e] == 0)
