@@ -558,21 +558,59 @@ def workload_name(name, r):
     return "%s fwd+bwd: T=%d H=%d I=%d E=%d top-%d %s" % (name, r.T, r.H, r.I, r.E, r.k, act)
 
 
+class _HostExperts(dict):
+    """Some experts' weights in host fp64, keyed by expert id; len() is the
+    number of experts of the layer (the oracle sizes its outputs by it)."""
+
+    def __init__(self, d, n_experts):
+        super().__init__(d)
+        self.n_experts = n_experts
+
+    def __len__(self):
+        return self.n_experts
+
+
 def run_reference(args, torch, synth):
     """Reference arm: the fp64 oracle on the host cores, each step a bounded
-    token sample of the same workload (inputs drawn on the GPU when present,
-    copied to the host one expert at a time)."""
+    token sample of the same workload.  The sample is the first tokens, as many
+    as fit the time budget (about two minutes for all steps) while touching at
+    most 16 experts; those experts' weights are moved to the host in fp64 once,
+    before the steps, so a step times the oracle's arithmetic only."""
+    import numpy as np
+    import oracle
     r = synth.RECIPES[args.workload]
     dev = "cuda" if torch.cuda.is_available() else "cpu"
     case = synth.make_case(r, device=dev)
-    per_step = max(1.0, 120.0 / max(1, args.steps + args.warmup))
-    n_tok = pick_sample(case, min(per_step, args.cpu_seconds))
+    idx_all = case.topk_idx.cpu().numpy().astype(np.int64)
+    n_max = 0
+    while n_max < r.T and len(np.unique(idx_all[:n_max + 1])) <= 16:
+        n_max += 1
+    n_max = max(1, n_max)
+    used = sorted(set(int(e) for e in np.unique(idx_all[:n_max])))
+    wgu = _HostExperts({e: case.w_gate_up[e].double().cpu().numpy() for e in used}, r.E)
+    wd = _HostExperts({e: case.w_down[e].double().cpu().numpy() for e in used}, r.E)
+    x_all = case.x[:n_max].double().cpu().numpy()
+    w_all = case.topk_w[:n_max].double().cpu().numpy()
+    dy_all = case.dy[:n_max].double().cpu().numpy()
+
+    def step(n):
+        ex = sorted(set(int(e) for e in np.unique(idx_all[:n])))
+        t0 = time.perf_counter()
+        oracle.moe_forward(x_all[:n], idx_all[:n], w_all[:n], wgu, wd, r.act, r.limit, r.alpha)
+        oracle.moe_backward(dy_all[:n], x_all[:n], idx_all[:n], w_all[:n], wgu, wd, r.act,
+                            r.limit, r.alpha, experts=ex)
+        return time.perf_counter() - t0
+
+    per_step = 120.0 / max(1, args.steps + args.warmup)
+    t1 = step(1)
+    n_tok = max(1, min(n_max, int(per_step / max(t1, 1e-3))))
     for _ in range(args.warmup):
-        oracle_step(case, n_tok)
-    t = sum(oracle_step(case, n_tok) for _ in range(args.steps))
+        step(n_tok)
+    t = sum(step(n_tok) for _ in range(args.steps))
     fs = layer_flops(r.scaled(T=n_tok))
     value = args.steps * (fs[0] + fs[1]) / t / 1e12
-    sample = "fp64 numpy oracle, fwd+bwd on the first %d of %d tokens per step" % (n_tok, r.T)
+    sample = ("fp64 numpy oracle, fwd+bwd on the first %d of %d tokens per step (%d experts' "
+              "weights, in host fp64 before the steps)" % (n_tok, r.T, len(set(idx_all[:n_tok].reshape(-1).tolist()))))
     out = {
         "metric": "MoE layer ms & TFLOP/s, % of bf16 tensor roofline (fwd and bwd)",
         "value": round(value, 5), "unit": "TFLOP/s", "n_gpus": args.gpus, "steps": args.steps,
