@@ -20,7 +20,7 @@ LIB = os.path.join(PKG, "libmoe_gb300.so")
 
 SOURCES = ["api.cu", "plan.cu", "permute.cu", "gemm_bf16_fwd.cu", "gemm_bf16_dgrad.cu",
            "gemm_bf16_wgrad.cu", "gemm_f32.cu", "plan_noalloc.cu", "route.cu"]
-HEADERS = ["common.cuh", "kernels.h", "gemm.cuh"]
+HEADERS = ["common.cuh", "kernels.h", "gemm.cuh", "abi_internal.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -18,6 +18,7 @@
 #include <mutex>
 #include <vector>
 
+#include "abi_internal.h"
 #include "kernels.h"
 #include "moe.h"
 
@@ -418,6 +419,27 @@ moe_status enqueue_gate_up(const moe_shape* s, const void* xp, const void* w_gat
 }
 
 }  // namespace
+
+// ------------------------------------------------------------ shared with other ABI units
+namespace moe {
+
+bool abi_shape_ok(const moe_shape* s) { return shape_ok(s); }
+
+moe_status abi_device_sms(int* sms) { return device_info(sms); }
+
+cudaError_t abi_tracked_plan(const int* idx, int64_t Tk, int E, int* counts, int* offsets,
+                             int* perm, int* inv, int* poff, int* blkhist, int* err,
+                             cudaStream_t st) {
+  return tracked(kKPlan, Tk > 0 ? 3 : 1, st, [&] {
+    return launch_plan(idx, Tk, E, counts, offsets, perm, inv, poff, blkhist, err, st);
+  });
+}
+
+cudaError_t abi_tracked_memset(void* p, int value, size_t bytes, cudaStream_t st) {
+  return tracked(kKMemset, 1, st, [&] { return cudaMemsetAsync(p, value, bytes, st); });
+}
+
+}  // namespace moe
 
 // ====================================================================== ABI
 extern "C" {

@@ -236,7 +236,12 @@ const char* moe_status_string(moe_status status);
  *     MOE_ERR_WORKSPACE without launching anything.
  *   - The first call on a device resolves the device address of the array
  *     (cudaGetSymbolAddress) with that device current; make that first call
- *     before any stream capture.
+ *     before any stream capture.  The address is kept per device context: a
+ *     call that finds a different context current (for instance after
+ *     cudaDeviceReset, which unloads the array) resolves it again, so such a
+ *     call, too, should come before any stream capture.
+ *   - Launches (three plan kernels and one memset of the error word) count in
+ *     moe_kernel_launch_count() and the event timer like moe_plan's.
  *   - Every call on a device shares the one array and leaves its contents
  *     behind; the call clears what must start at zero.  Calls whose kernels
  *     may overlap on the GPU (different streams, or different host threads)

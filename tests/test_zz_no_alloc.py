@@ -61,3 +61,28 @@ def test_plan_noalloc_refuses_oversized_problem():
     _, out_s = m.alloc_plan(m.Shape(1, 64, 64, 1024, 8))
     st = fn(ctypes.byref(shape), 16, ctypes.byref(out_s), torch.cuda.current_stream().cuda_stream)
     assert st == m.MOE_ERR_WORKSPACE
+
+
+def test_plan_noalloc_wrapper_bad_id_and_launch_count():
+    """Through the package wrapper: one expert id set to E on the host (an id
+    the plan must leave out) is detectable as offsets[E] == T*k - 1, the
+    valid ids are counted exactly, and the call's three kernels and one
+    memset show in the launch counter."""
+    import dispatch_gemm_combine_gb300 as m
+    T, k, E = 900, 4, 32
+    r = Recipe("t", T=T, H=64, I=64, E=E, k=k, act=ACT_SWIGLU, weight_std="fan_in",
+               routing="uniform_ids", seed=31)
+    idx_h = synth.make_case(r, with_dy=False).topk_idx.clone()
+    idx_h[17, 2] = E
+    idx = idx_h.cuda()
+    shape = m.Shape(T, 64, 64, E, k)
+    out_t, out_s = m.alloc_plan(shape)
+    n0 = m.moe_kernel_launch_count()
+    st = m.moe_plan_noalloc(shape, idx.data_ptr(), out_s, torch.cuda.current_stream().cuda_stream)
+    assert st == m.MOE_OK, m.moe_status_string(st)
+    assert m.moe_kernel_launch_count() - n0 == 4
+    torch.cuda.synchronize()
+    assert int(out_t["offsets"][E].item()) == T * k - 1
+    valid = idx_h.reshape(-1).numpy()
+    want = np.bincount(valid[valid < E], minlength=E)
+    assert np.array_equal(out_t["counts"].cpu().numpy(), want)
