@@ -211,33 +211,59 @@ def summarize_clocks(lines):
 # ---------------------------------------------------------------- CPU oracle leg
 
 
-class _LazyExperts:
-    """Expert weights fetched from the device one expert at a time (fp32)."""
+class _HostExperts(dict):
+    """Some experts' weights in host fp64, keyed by expert id; len() is the
+    number of experts of the layer (the oracle sizes its outputs by it)."""
 
-    def __init__(self, t):
-        self.t = t
+    def __init__(self, d, n_experts):
+        super().__init__(d)
+        self.n_experts = n_experts
 
     def __len__(self):
-        return self.t.shape[0]
-
-    def __getitem__(self, e):
-        return self.t[e].float().cpu().numpy()
+        return self.n_experts
 
 
-def oracle_step(case, n_tok):
-    """One fp64 oracle pass (forward + backward) over the first n_tok tokens."""
-    import numpy as np
-    import oracle
-    r = case.recipe
-    x = case.x[:n_tok].float().cpu().numpy()
-    idx = case.topk_idx[:n_tok].cpu().numpy().astype(np.int64)
-    w = case.topk_w[:n_tok].cpu().numpy()
-    dy = case.dy[:n_tok].float().cpu().numpy()
-    wgu, wd = _LazyExperts(case.w_gate_up), _LazyExperts(case.w_down)
-    t0 = time.perf_counter()
-    oracle.moe_forward(x, idx, w, wgu, wd, r.act, r.limit, r.alpha)
-    oracle.moe_backward(dy, x, idx, w, wgu, wd, r.act, r.limit, r.alpha)
-    return time.perf_counter() - t0
+class OracleSample:
+    """A bounded sample of a workload for timing the fp64 oracle on the host:
+    the first tokens of the case, as many as touch at most `max_experts`
+    experts.  Everything the oracle reads (those tokens' rows and routing and
+    the touched experts' weights) is converted to host fp64 once, here, so a
+    timed pass runs the oracle's arithmetic only.  The cpu_baseline leg and
+    the reference arm both use this sample, so their per-token rates agree."""
+
+    def __init__(self, case, max_experts=16):
+        import numpy as np
+        r = case.recipe
+        self.r = r
+        idx_all = case.topk_idx.cpu().numpy().astype(np.int64)
+        n = 0
+        while n < r.T and len(np.unique(idx_all[:n + 1])) <= max_experts:
+            n += 1
+        self.n_max = max(1, n)
+        self.idx = idx_all[:self.n_max]
+        used = sorted(set(int(e) for e in np.unique(self.idx)))
+        self.wgu = _HostExperts({e: case.w_gate_up[e].double().cpu().numpy() for e in used}, r.E)
+        self.wd = _HostExperts({e: case.w_down[e].double().cpu().numpy() for e in used}, r.E)
+        self.x = case.x[:self.n_max].double().cpu().numpy()
+        self.w = case.topk_w[:self.n_max].double().cpu().numpy()
+        self.dy = case.dy[:self.n_max].double().cpu().numpy()
+
+    def experts(self, n):
+        import numpy as np
+        return sorted(set(int(e) for e in np.unique(self.idx[:n])))
+
+    def step(self, n):
+        """One fp64 oracle pass (forward + backward) over the first n sampled
+        tokens; returns its wall time in seconds."""
+        import oracle
+        r = self.r
+        ex = self.experts(n)
+        t0 = time.perf_counter()
+        oracle.moe_forward(self.x[:n], self.idx[:n], self.w[:n], self.wgu, self.wd, r.act,
+                           r.limit, r.alpha)
+        oracle.moe_backward(self.dy[:n], self.x[:n], self.idx[:n], self.w[:n], self.wgu, self.wd,
+                            r.act, r.limit, r.alpha, experts=ex)
+        return time.perf_counter() - t0
 
 
 def cpu_cores():
@@ -247,12 +273,135 @@ def cpu_cores():
         return os.cpu_count()
 
 
-def pick_sample(case, target_s):
-    """Token count whose oracle pass takes about target_s seconds."""
-    n = 64
-    t = oracle_step(case, n)
-    n2 = int(n * target_s / max(t, 1e-3))
-    return max(16, min(case.recipe.T, n2))
+def cpu_model():
+    """The host CPU's model name (lscpu, else /proc/cpuinfo), or the machine type."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith(("model name", "cpu part")):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    import platform
+    return platform.machine()
+
+
+def cpu_baseline(case, target_s):
+    """The oracle timed on the host cores over OracleSample's tokens, repeated
+    until about target_s seconds of CPU work have been timed."""
+    smp = OracleSample(case)
+    n = smp.n_max
+    t1 = smp.step(n)
+    reps = max(1, int(round(target_s / max(t1, 1e-3))))
+    t = sum(smp.step(n) for _ in range(reps))
+    fs = layer_flops(case.recipe.scaled(T=n))
+    return {"value": round(reps * (fs[0] + fs[1]) / t / 1e12, 5), "unit": "TFLOP/s",
+            "cores": cpu_cores(), "kind": "oracle",
+            "sample": "fp64 numpy oracle on %s: fwd+bwd over the first %d of %d tokens (the "
+                      "prefix touching at most 16 experts; their weights in host fp64 before the "
+                      "clock), %d passes, %.1f s" % (cpu_model(), n, case.recipe.T, reps, t)}
+
+
+def stats_ms(samples):
+    """Median, p10 and p90 of per-call times in ms."""
+    xs = sorted(samples)
+
+    def q(p):
+        if not xs:
+            return None
+        pos = p * (len(xs) - 1)
+        lo = int(pos)
+        hi = min(lo + 1, len(xs) - 1)
+        return xs[lo] + (xs[hi] - xs[lo]) * (pos - lo)
+
+    return {"median": round(q(0.5), 4), "p10": round(q(0.1), 4), "p90": round(q(0.9), 4),
+            "n": len(xs)}
+
+
+def timed_calls(fn, n, stream):
+    """Run fn n times on `stream` with an event pair around each call; returns
+    the per-call device times in ms."""
+    import torch
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(n + 1)]
+    evs[0].record(stream)
+    for i in range(n):
+        fn()
+        evs[i + 1].record(stream)
+    torch.cuda.synchronize()
+    return [evs[i].elapsed_time(evs[i + 1]) for i in range(n)]
+
+
+# ---------------------------------------------------------------- other configs
+
+# The workloads reported beside the bench line: the SwiGLU forward and
+# backward shapes and the load-imbalance sweep on the backward shape.
+CONFIG_RUNS = [("swiglu_fwd", None), ("swiglu_bwd", None)] + \
+    [("zipf_sweep", T) for T in (512, 2048, 8192, 16384)]
+
+
+def measure_configs(synth, LayerRunner, stream, P, BW, peak_src, n_calls=10, warm=2):
+    """Per workload: training forward, inference forward and backward, each
+    timed per call (median, p10, p90 over n_calls after `warm` untimed
+    calls), with each half's fraction of its roofline max(FLOPs / P, bytes /
+    BW) at the median."""
+    import torch
+    from dispatch_gemm_combine_gb300 import MOE_BF16
+    res = {}
+    for name, T in CONFIG_RUNS:
+        r = synth.RECIPES[name]
+        if T is not None:
+            r = r.scaled(T=T)
+        case = synth.make_case(r, device="cuda")
+        run = LayerRunner(r.T, r.H, r.I, r.E, r.k, r.act, MOE_BF16, r.limit, r.alpha)
+        a = (case.x, case.topk_idx, case.topk_w, case.w_gate_up, case.w_down)
+
+        def fwd(inference=False):
+            run.plan(case.topk_idx)
+            run.forward(*a, inference=inference)
+
+        def bwd():
+            run.backward(case.dy, *a)
+
+        for _ in range(warm):
+            fwd()
+            bwd()
+        fc = timed_calls(fwd, n_calls, stream)
+        ic = timed_calls(lambda: fwd(True), n_calls, stream)
+        fwd()   # the saved context of a training forward for the backward calls
+        bc = timed_calls(bwd, n_calls, stream)
+        run.check()
+        e_active = int((run.plan_t["counts"] > 0).sum().item())
+        zero, ratio = synth.routing_stats(case.topk_idx, r.E)
+        f_fwd, f_bwd = layer_flops(r)
+        b_fwd, b_bwd = layer_bytes(r, e_active)
+
+        def part(calls, flops, byts):
+            m = statistics.median(calls)
+            roof = max(flops / P, byts / BW) * 1e3
+            return {"ms": stats_ms(calls), "tflops": round(flops / (m * 1e-3) / 1e12, 1),
+                    "frac": round(roof / m, 4), "bound": "tensor" if flops / P > byts / BW else "hbm"}
+
+        key = name if T is None else "%s_T%d" % (name, T)
+        fp = part(fc, f_fwd, b_fwd)
+        bp = part(bc, f_bwd, b_bwd)
+        res[key] = {"workload": workload_name(name, r), "fwd": fp,
+                    "fwd_inference": part(ic, f_fwd, b_fwd), "bwd": bp,
+                    "step_ms": round(fp["ms"]["median"] + bp["ms"]["median"], 4),
+                    "tflops": round((f_fwd + f_bwd) / ((fp["ms"]["median"] + bp["ms"]["median"])
+                                                       * 1e-3) / 1e12, 1),
+                    "experts_active": e_active, "experts_empty_frac": round(zero, 3),
+                    "hottest_over_mean": round(ratio, 2)}
+        del run, case, a
+        torch.cuda.empty_cache()
+    res["peaks"] = "%s: P = %.1f TFLOP/s sustained bf16, BW = %.1f GB/s" % (peak_src, P / 1e12,
+                                                                           BW / 1e9)
+    return res
 
 
 # ---------------------------------------------------------------- main
@@ -268,6 +417,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="target length of the oracle sample (cpu_baseline)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the per-workload table of the other synthetic configs")
     ap.add_argument("--tokens", type=int, default=None,
                     help="run the workload at this many tokens (the load-imbalance sweep's T "
                          "values); the bench line itself uses the workload's own T")
@@ -330,17 +481,19 @@ def main():
     barrier()
     torch.cuda.synchronize()
     n0 = moe_kernel_launch_count()
-    ev0 = torch.cuda.Event(enable_timing=True)
-    ev1 = torch.cuda.Event(enable_timing=True)
-    ev0.record(stream)
-    for _ in range(args.steps):
+    # one event before the first step and one after each step (same stream):
+    # the whole region gives the mean, the gaps give per-step percentiles
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    evs[0].record(stream)
+    for i in range(args.steps):
         step()
-    ev1.record(stream)
+        evs[i + 1].record(stream)
     torch.cuda.synchronize()
     barrier()
     launches = moe_kernel_launch_count() - n0
     clocks.stop()
-    ms = ranks_max(ev0.elapsed_time(ev1)) / args.steps
+    ms = ranks_max(evs[0].elapsed_time(evs[-1])) / args.steps
+    step_stats = stats_ms([evs[i].elapsed_time(evs[i + 1]) for i in range(args.steps)])
     run.check()
 
     # ---- per-kernel times (separate pass, library event timer on the same stream)
@@ -353,29 +506,31 @@ def main():
     prof = moe_profile_read()
     moe_profile_enable(False)
 
-    # ---- fwd / bwd split
+    # ---- fwd / bwd split: per-call device times (median, p10, p90)
     def timed(fn, n):
-        a = torch.cuda.Event(enable_timing=True)
-        b = torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        for _ in range(n):
-            fn()
-        b.record(stream)
-        torch.cuda.synchronize()
-        return a.elapsed_time(b) / n
+        return statistics.mean(timed_calls(fn, n, stream))
 
     n_split = max(3, min(args.steps, 20))
-    fwd_ms = timed(lambda: (run.plan(case.topk_idx),
-                            run.forward(case.x, case.topk_idx, case.topk_w, case.w_gate_up,
-                                        case.w_down)), n_split)
-    bwd_ms = timed(lambda: run.backward(case.dy, case.x, case.topk_idx, case.topk_w,
-                                        case.w_gate_up, case.w_down), n_split)
+    fwd_calls = timed_calls(lambda: (run.plan(case.topk_idx),
+                                     run.forward(case.x, case.topk_idx, case.topk_w,
+                                                 case.w_gate_up, case.w_down)), n_split, stream)
+    bwd_calls = timed_calls(lambda: run.backward(case.dy, case.x, case.topk_idx, case.topk_w,
+                                                 case.w_gate_up, case.w_down), n_split, stream)
+    # inference-mode forward: no context saved for a backward
+    inf_calls = timed_calls(lambda: (run.plan(case.topk_idx),
+                                     run.forward(case.x, case.topk_idx, case.topk_w,
+                                                 case.w_gate_up, case.w_down, inference=True)),
+                            n_split, stream)
+    fwd_ms = statistics.median(fwd_calls)
+    bwd_ms = statistics.median(bwd_calls)
     # the memory-lean backward: no saved context, recomputed inside
     run.backward(case.dy, case.x, case.topk_idx, case.topk_w, case.w_gate_up, case.w_down,
                  recompute=True)
-    bwd_re_ms = timed(lambda: run.backward(case.dy, case.x, case.topk_idx, case.topk_w,
-                                           case.w_gate_up, case.w_down, recompute=True), n_split)
-
+    bwd_re_ms = statistics.median(timed_calls(
+        lambda: run.backward(case.dy, case.x, case.topk_idx, case.topk_w, case.w_gate_up,
+                             case.w_down, recompute=True), n_split, stream))
+    # the layer's forward output for the e2e check below (the inference
+    # forward above left the same y)
     # ---- end to end: pinned host inputs in, per-token results out, every step.
     # As a training input pipeline runs it: a copy stream brings step i+1's
     # inputs in and step i's results out while step i+1 computes, with two sets
@@ -523,8 +678,15 @@ def main():
                    "parallelism": "replicas" if world > 1 else "single GPU",
                    "l2": "no flush: %.1f GB of expert weights per step exceed the 129 MB L2"
                          % (r.E * 3 * r.H * r.I * case.w_down.element_size() / 1e9)},
-        "layer": {"fwd": layer_part(fwd_ms, f_fwd, b_fwd), "bwd": layer_part(bwd_ms, f_bwd, b_bwd),
-                  "bwd_recompute_ms": round(bwd_re_ms, 4)},
+        "step_ms": step_stats,
+        "layer": {"fwd": dict(layer_part(fwd_ms, f_fwd, b_fwd), **{"calls": stats_ms(fwd_calls)}),
+                  "fwd_inference": dict(layer_part(statistics.median(inf_calls), f_fwd, b_fwd),
+                                        **{"calls": stats_ms(inf_calls)}),
+                  "bwd": dict(layer_part(bwd_ms, f_bwd, b_bwd), **{"calls": stats_ms(bwd_calls)}),
+                  "bwd_recompute_ms": round(bwd_re_ms, 4),
+                  "timing": "fwd = plan + training forward (saves the context), fwd_inference = "
+                            "plan + forward without it, bwd = backward from the saved context; "
+                            "ms and frac use the median call"},
         "roofline": roofline,
         "kernels": per_kernel,
         "e2e": {"value": round(job_throughput(step_flops, world, e2e_ms), 2), "unit": "TFLOP/s",
@@ -539,13 +701,13 @@ def main():
         "experts_active": e_active,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        n_tok = pick_sample(case, args.cpu_seconds)
-        t = oracle_step(case, n_tok)
-        fs = layer_flops(r.scaled(T=n_tok))
-        out["cpu_baseline"] = {"value": round((fs[0] + fs[1]) / t / 1e12, 5), "unit": "TFLOP/s",
-                               "cores": cpu_cores(), "kind": "oracle",
-                               "sample": "fp64 numpy oracle, fwd+bwd on the first %d of %d tokens "
-                                         "(all experts' weights), %.1f s" % (n_tok, r.T, t)}
+        out["cpu_baseline"] = cpu_baseline(case, args.cpu_seconds)
+    if not args.no_configs and args.tokens is None and args.experts is None:
+        # the other synthetic workloads, each on its own buffers (the bench
+        # workload's are released first)
+        del runs, d_in, run, case
+        torch.cuda.empty_cache()
+        out["configs"] = measure_configs(synth, LayerRunner, stream, P, BW, peak_src)
     if rank == 0:
         print(json.dumps(out))
     if world > 1:
@@ -558,59 +720,26 @@ def workload_name(name, r):
     return "%s fwd+bwd: T=%d H=%d I=%d E=%d top-%d %s" % (name, r.T, r.H, r.I, r.E, r.k, act)
 
 
-class _HostExperts(dict):
-    """Some experts' weights in host fp64, keyed by expert id; len() is the
-    number of experts of the layer (the oracle sizes its outputs by it)."""
-
-    def __init__(self, d, n_experts):
-        super().__init__(d)
-        self.n_experts = n_experts
-
-    def __len__(self):
-        return self.n_experts
-
-
 def run_reference(args, torch, synth):
     """Reference arm: the fp64 oracle on the host cores, each step a bounded
-    token sample of the same workload.  The sample is the first tokens, as many
-    as fit the time budget (about two minutes for all steps) while touching at
-    most 16 experts; those experts' weights are moved to the host in fp64 once,
-    before the steps, so a step times the oracle's arithmetic only."""
-    import numpy as np
-    import oracle
+    token sample of the same workload (OracleSample: the prefix of tokens that
+    touches at most 16 experts, their weights in host fp64 before the steps),
+    as many of those tokens as fit about two minutes for all steps."""
     r = synth.RECIPES[args.workload]
     dev = "cuda" if torch.cuda.is_available() else "cpu"
     case = synth.make_case(r, device=dev)
-    idx_all = case.topk_idx.cpu().numpy().astype(np.int64)
-    n_max = 0
-    while n_max < r.T and len(np.unique(idx_all[:n_max + 1])) <= 16:
-        n_max += 1
-    n_max = max(1, n_max)
-    used = sorted(set(int(e) for e in np.unique(idx_all[:n_max])))
-    wgu = _HostExperts({e: case.w_gate_up[e].double().cpu().numpy() for e in used}, r.E)
-    wd = _HostExperts({e: case.w_down[e].double().cpu().numpy() for e in used}, r.E)
-    x_all = case.x[:n_max].double().cpu().numpy()
-    w_all = case.topk_w[:n_max].double().cpu().numpy()
-    dy_all = case.dy[:n_max].double().cpu().numpy()
-
-    def step(n):
-        ex = sorted(set(int(e) for e in np.unique(idx_all[:n])))
-        t0 = time.perf_counter()
-        oracle.moe_forward(x_all[:n], idx_all[:n], w_all[:n], wgu, wd, r.act, r.limit, r.alpha)
-        oracle.moe_backward(dy_all[:n], x_all[:n], idx_all[:n], w_all[:n], wgu, wd, r.act,
-                            r.limit, r.alpha, experts=ex)
-        return time.perf_counter() - t0
-
+    smp = OracleSample(case)
     per_step = 120.0 / max(1, args.steps + args.warmup)
-    t1 = step(1)
-    n_tok = max(1, min(n_max, int(per_step / max(t1, 1e-3))))
+    t1 = smp.step(1)
+    n_tok = max(1, min(smp.n_max, int(per_step / max(t1, 1e-3))))
     for _ in range(args.warmup):
-        step(n_tok)
-    t = sum(step(n_tok) for _ in range(args.steps))
+        smp.step(n_tok)
+    t = sum(smp.step(n_tok) for _ in range(args.steps))
     fs = layer_flops(r.scaled(T=n_tok))
     value = args.steps * (fs[0] + fs[1]) / t / 1e12
-    sample = ("fp64 numpy oracle, fwd+bwd on the first %d of %d tokens per step (%d experts' "
-              "weights, in host fp64 before the steps)" % (n_tok, r.T, len(set(idx_all[:n_tok].reshape(-1).tolist()))))
+    sample = ("fp64 numpy oracle on %s: fwd+bwd over the first %d of %d tokens per step (%d "
+              "experts' weights, in host fp64 before the steps)"
+              % (cpu_model(), n_tok, r.T, len(smp.experts(n_tok))))
     out = {
         "metric": "MoE layer ms & TFLOP/s, % of bf16 tensor roofline (fwd and bwd)",
         "value": round(value, 5), "unit": "TFLOP/s", "n_gpus": args.gpus, "steps": args.steps,

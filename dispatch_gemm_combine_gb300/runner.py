@@ -42,12 +42,14 @@ class LayerRunner:
         route(self.shape, logits, topk_idx, topk_w, self.plan_s, self.ws_plan, stream)
 
     def forward(self, x, topk_idx, topk_w, w_gate_up, w_down, use_plan=True, stream=None,
-                b_gate_up=None, b_down=None):
+                b_gate_up=None, b_down=None, inference=False):
         """y = layer(x).  With use_plan the plan must have been built by plan();
         otherwise the forward builds its own inside the workspace.  b_gate_up
-        [E,2I] / b_down [E,H] (storage dtype) are the optional per-expert biases."""
+        [E,2I] / b_down [E,H] (storage dtype) are the optional per-expert biases.
+        inference=True saves no context for the backward (as a runner built
+        with training=False)."""
         ffn_fwd(self.shape, x, topk_idx, topk_w, w_gate_up, w_down, self.y, self.ws_fwd,
-                self.plan_s if use_plan else None, self.saved, stream,
+                self.plan_s if use_plan else None, None if inference else self.saved, stream,
                 bias_struct(b_gate_up, b_down))
         return self.y
 

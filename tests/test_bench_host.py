@@ -97,3 +97,24 @@ def test_zipf_routing_stats():
     # each token picks k distinct experts
     ids = case.topk_idx
     assert all(len(set(row.tolist())) == r.k for row in ids)
+
+
+def test_stats_ms_percentiles():
+    s = bench.stats_ms([float(v) for v in range(1, 12)])   # 1 .. 11 ms
+    assert s["median"] == 6.0 and s["p10"] == 2.0 and s["p90"] == 10.0 and s["n"] == 11
+
+
+def test_oracle_sample_is_bounded_and_consistent():
+    """The CPU sample used by cpu_baseline and by the reference arm: a token
+    prefix touching at most max_experts experts, whose timed passes run the
+    oracle on host fp64 copies made beforehand."""
+    r = synth.RECIPES["clamped_glu_fwd"].scaled(T=64, H=64, I=64, E=32)
+    case = synth.make_case(r)
+    smp = bench.OracleSample(case, max_experts=6)
+    assert 1 <= smp.n_max <= r.T
+    assert len(smp.experts(smp.n_max)) <= 6
+    if smp.n_max < r.T:   # the next token would bring in a seventh expert
+        nxt = set(case.topk_idx[:smp.n_max + 1].reshape(-1).tolist())
+        assert len(nxt) > 6
+    assert set(smp.wgu) == set(smp.experts(smp.n_max))
+    assert smp.step(smp.n_max) > 0.0

@@ -34,7 +34,8 @@ class LazyExperts:
         return self.t.shape[0]
 
     def __getitem__(self, e):
-        return self.t[int(e)].cpu().double().numpy()
+        # widened on the device (exact), so the host receives fp64 directly
+        return self.t[int(e)].double().cpu().numpy()
 
 
 def _run(r, backward, biases=None):
@@ -80,13 +81,18 @@ def _check_tokens(case, y, grads, n_tok, seed):
         assert_dw_close(dtw[toks].cpu().numpy(), dw_ref)
 
 
-def _check_expert_grads(case, run, grads, n_exp, seed, max_rows=4096):
+def _check_expert_grads(case, run, grads, n_exp, seed, max_rows=4096, hottest=False):
+    """Weight gradients of n_exp sampled experts (among those with at most
+    max_rows rows), and with hottest=True also of the expert holding the most
+    rows, element by element against the oracle on exactly their tokens."""
     r = case.recipe
     counts = run.plan_t["counts"].cpu().numpy()
     live = [e for e in range(r.E) if 0 < counts[e] <= max_rows]
     g = np.random.default_rng(seed)
-    for e in g.choice(live, size=min(n_exp, len(live)), replace=False):
-        e = int(e)
+    picks = [int(e) for e in g.choice(live, size=min(n_exp, len(live)), replace=False)]
+    if hottest:
+        picks.append(int(np.argmax(counts)))
+    for e in picks:
         toks = torch.nonzero((case.topk_idx == e).any(dim=1)).flatten().cpu()
         x, idx, w, dy = _host(case, toks)
         wgu, wd = LazyExperts(case.w_gate_up), LazyExperts(case.w_down)
@@ -127,7 +133,7 @@ def test_clamped_glu_workload_fwd_bwd():
 def test_swiglu_forward_workload():
     """T=4096, H=8192, I=2048, 256 experts, top-8 (26 GB of weights)."""
     case, run, y, _ = _run(synth.RECIPES["swiglu_fwd"], backward=False)
-    _check_tokens(case, y, None, n_tok=6, seed=3)
+    _check_tokens(case, y, None, n_tok=32, seed=3)
 
 
 def test_swiglu_backward_workload():
@@ -147,7 +153,9 @@ def test_zipf_sweep(T):
     zero, ratio = synth.routing_stats(case.topk_idx, r.E)
     assert zero >= 0.25 and ratio > 10.0, (zero, ratio)
     _check_tokens(case, y, grads, n_tok=6, seed=T)
-    _check_expert_grads(case, run, grads, n_exp=1, seed=T + 1, max_rows=2048)
+    # a sampled expert plus the hottest one (about 0.9 T rows at this routing:
+    # the longest weight-gradient contraction of the sweep)
+    _check_expert_grads(case, run, grads, n_exp=1, seed=T + 1, max_rows=2048, hottest=True)
     _check_identities(case, y, grads)
 
 
