@@ -138,6 +138,7 @@ struct TileInfo {
   bool active; // false when this CTA's 128 rows lie past the expert (or the output)
   bool half;   // row-grouped pair unit of one 128-row tile (64 rows per CTA, M = 128)
   int nn;      // token-N tiling: tokens (N) of this unit, a multiple of 16
+  bool lo;     // bf16 backward: this expert's computed operand carries its bf16 remainder
 };
 
 // Work unit t of the schedule.  A unit is PAIR consecutive m-tiles with one
@@ -150,11 +151,13 @@ __device__ __forceinline__ TileInfo decode_tile(const GemmArgs& a, int t, int bk
   TileInfo ti;
   ti.half = false;
   ti.nn = 0;
+  ti.lo = true;
   const int NT = a.n_tiles;
   if constexpr (kWgrad) {
     const int MP = (a.m_tiles + PAIR - 1) / PAIR;
     const int per_e = MP * NT;
     ti.e = t / per_e;
+    if (a.lo_flags) ti.lo = __ldg(a.lo_flags + ti.e) != 0;
     const int r = t - ti.e * per_e;
     const int mp = r / NT;
     ti.nt = r - mp * NT;
@@ -180,6 +183,7 @@ __device__ __forceinline__ TileInfo decode_tile(const GemmArgs& a, int t, int bk
         hi = mid - 1;
     }
     ti.e = lo;
+    if (a.lo_flags) ti.lo = __ldg(a.lo_flags + lo) != 0;
     const int p0 = __ldg(a.poff + lo);
     const int mt = (__ldg(a.poff + lo + 1) - p0) >> 7;
     const int mu = ((__ldg(up + lo + 1) - __ldg(up + lo)) >> sh);   // units of m
@@ -546,7 +550,10 @@ __global__ void __launch_bounds__(192, 1)
           // token-N tiling: a unit of at most 64 tokens (32 rows per CTA)
           // loads its token rows with the 32-row box of maps.a2
           const bool small_b = C::SW && ti.nn <= 64;
-          const uint32_t stage_tx = small_b ? C::A_BYTES + 32 * 128 : C::STAGE_BYTES;
+          // a split operand's lo part is loaded only for experts that need it
+          constexpr uint32_t kLoBytes = C::SPLIT_A ? C::A_PART : (C::SPLIT_B ? C::B_PART : 0);
+          const uint32_t stage_tx = small_b ? C::A_BYTES + 32 * 128
+                                            : C::STAGE_BYTES - (ti.lo ? 0u : kLoBytes);
           // the leader expects the bytes of both CTAs of the pair
           if (leader) mbar_arrive_expect_tx(fb, C::PAIR * stage_tx);
           auto load2 = [&](uint32_t dst, const CUtensorMap* m, int c0, int c1) {
@@ -583,11 +590,13 @@ __global__ void __launch_bounds__(192, 1)
           } else {
             // MN-major chunks (128 B of M x BK rows): hi, then lo when split
 #pragma unroll
-            for (int part = 0; part < (C::SPLIT_A ? 2 : 1); ++part)
+            for (int part = 0; part < (C::SPLIT_A ? 2 : 1); ++part) {
+              if (part && !ti.lo) break;
 #pragma unroll
               for (int c = 0; c < 128 / C::CH; ++c)
                 load2(sA + part * C::A_PART + c * C::CHUNK_BYTES, part ? &maps.a2 : &maps.a,
                       ti.m0 + c * C::CH, ti.row0 + kc);
+            }
           }
           // ---- B: this CTA's BN_CTA columns
           const int nb = ti.n0 + crank * C::BN_CTA;
@@ -622,11 +631,13 @@ __global__ void __launch_bounds__(192, 1)
             load2(sB, &maps.b0, ti.row0 + kc, nb);
           } else {
 #pragma unroll
-            for (int part = 0; part < (C::SPLIT_B ? 2 : 1); ++part)
+            for (int part = 0; part < (C::SPLIT_B ? 2 : 1); ++part) {
+              if (part && !ti.lo) break;
 #pragma unroll
               for (int c = 0; c < C::BN_CTA / C::CH; ++c)
                 load2(sB + part * C::B_PART + c * C::CHUNK_BYTES, part ? &maps.b1 : &maps.b0,
                       nb + c * C::CH, ti.row0 + kc);
+            }
           }
           }
         }
@@ -703,9 +714,9 @@ __global__ void __launch_bounds__(192, 1)
               const uint64_t bdesc = smem_desc_sw128(sB + boff, blbo, 1024);
               mma(adesc, bdesc, (kb | kk) != 0 ? 1u : 0u);
               if constexpr (C::SPLIT_A)
-                mma(smem_desc_sw128(sA + C::A_PART + aoff, albo, 1024), bdesc, 1u);
+                if (ti.lo) mma(smem_desc_sw128(sA + C::A_PART + aoff, albo, 1024), bdesc, 1u);
               if constexpr (C::SPLIT_B)
-                mma(adesc, smem_desc_sw128(sB + C::B_PART + boff, blbo, 1024), 1u);
+                if (ti.lo) mma(adesc, smem_desc_sw128(sB + C::B_PART + boff, blbo, 1024), 1u);
             }
             // the stage is free in both CTAs once these MMAs have read it
             if constexpr (C::CTA2)
@@ -1074,7 +1085,8 @@ __global__ void __launch_bounds__(192, 1)
                 store_tile<T>(args.out[2], 0, orow, i0, aw, my_epi, lane);
               } else if constexpr (C::IL) {
                 // dgate / dup of output i are columns 2i, 2i + 1 of dH1: bf16
-                // hi parts, then the remainders, of 16 outputs at a time
+                // hi parts, then (for experts that need them) the remainders,
+                // of 16 outputs at a time
 #pragma unroll
                 for (int hh = 0; hh < 2; ++hh) {
                   float t[32];
@@ -1084,18 +1096,27 @@ __global__ void __launch_bounds__(192, 1)
                     t[2 * p + 1] = bf16_round(du[16 * hh + p]);
                   }
                   store_tile<T>(args.out[0], 0, orow, 2 * i0 + 32 * hh, t, my_epi, lane);
+                  if (ti.lo) {
 #pragma unroll
-                  for (int p = 0; p < 16; ++p) {
-                    t[2 * p] = dg[16 * hh + p] - bf16_round(dg[16 * hh + p]);
-                    t[2 * p + 1] = du[16 * hh + p] - bf16_round(du[16 * hh + p]);
+                    for (int p = 0; p < 16; ++p) {
+                      t[2 * p] = dg[16 * hh + p] - bf16_round(dg[16 * hh + p]);
+                      t[2 * p + 1] = du[16 * hh + p] - bf16_round(du[16 * hh + p]);
+                    }
+                    store_tile<T>(args.out[3], 0, orow, 2 * i0 + 32 * hh, t, my_epi, lane);
                   }
-                  store_tile<T>(args.out[3], 0, orow, 2 * i0 + 32 * hh, t, my_epi, lane);
                 }
-                float lo[32];
+                if (ti.lo) {
+                  float lo[32];
 #pragma unroll
-                for (int i = 0; i < 32; ++i) split_bf16(aw[i], aw[i], lo[i]);
+                  for (int i = 0; i < 32; ++i) split_bf16(aw[i], aw[i], lo[i]);
+                  store_tile<T>(args.out[5], 0, orow, i0, lo, my_epi, lane);
+                }
                 store_tile<T>(args.out[2], 0, orow, i0, aw, my_epi, lane);
-                store_tile<T>(args.out[5], 0, orow, i0, lo, my_epi, lane);
+              } else if (!ti.lo) {
+                // one bf16 value per operand (the store rounds to nearest)
+                store_tile<T>(args.out[0], 0, orow, i0, dg, my_epi, lane);
+                store_tile<T>(args.out[1], 0, orow, i0, du, my_epi, lane);
+                store_tile<T>(args.out[2], 0, orow, i0, aw, my_epi, lane);
               } else {
                 // bf16 hi parts (operands of the dgrad and the wgrads) and lo
                 // parts (the remainders, operands of the wgrads only)

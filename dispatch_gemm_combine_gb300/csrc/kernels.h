@@ -58,11 +58,18 @@ cudaError_t launch_bias_slot_dot(const void* dy, const void* b_down, int H, int 
 // out[e, c] = sum_{j < counts[e]} s_j * (src[r_j, c] (+ src2[r_j, c])) in fp32,
 // in a fixed order; r_j = poff[e] + j, or perm[offsets[e] + j] / gather_k when
 // gather_k > 0; s_j = topk_w[perm[offsets[e] + j]] when `weighted`, else 1.
-// src / src2 (optional) have row stride ld; C % 8 == 0.
+// src / src2 (optional) have row stride ld; C % 8 == 0.  With src2_flags,
+// src2 is read only for experts whose flag is non-zero.
 cudaError_t launch_expert_colsum(const void* src, const void* src2, int C, int64_t ld,
                                  int gather_k, int E, const int* poff, const int* counts,
                                  const int* offsets, const int* perm, const float* topk_w, int tk,
-                                 bool weighted, float* out, int elem_bytes, cudaStream_t st);
+                                 bool weighted, const int* src2_flags, float* out, int elem_bytes,
+                                 cudaStream_t st);
+// lo_flags[e] = 0 when expert e's effective row count (sum w^2)^2 / sum w^4
+// over its routing weights is at least min_neff (its weight gradients then
+// take the computed operand as one bf16 value), else 1 (bf16 hi + lo parts).
+cudaError_t launch_split_select(const int* offsets, const int* perm, const float* topk_w, int tk,
+                                int E, float min_neff, int* lo_flags, cudaStream_t st);
 
 // ---- grouped tensor-core GEMMs (gemm_*.cu)
 enum GemmMode : int {
@@ -104,6 +111,9 @@ struct GemmArgs {
   const void* h1;       // kDgradDown: saved pre-activations [rows_max, 2I]
   int I;
   float* dwpart;        // kDgradDown: [n_tiles][rows_max]
+  const int* lo_flags;  // bf16 backward: per expert, 1 = its weight gradients use the bf16
+                        // hi + lo parts of the computed operand, 0 = the hi part alone (the
+                        // down dgrad then writes no lo part); null = always both
   int64_t rows_max;
   int* err;
   uint64_t timeout_ns;

@@ -248,9 +248,12 @@ __global__ void __launch_bounds__(64 * kRowGroups) expert_colsum_kernel(
     const T* __restrict__ src, const T* __restrict__ src2, int C, int64_t ld, int gather_k,
     const int* __restrict__ poff, const int* __restrict__ counts,
     const int* __restrict__ offsets, const int* __restrict__ perm,
-    const float* __restrict__ topk_w, int tk, int weighted, float* __restrict__ out) {
+    const float* __restrict__ topk_w, int tk, int weighted, const int* __restrict__ src2_flags,
+    float* __restrict__ out) {
   __shared__ float4 part[kRowGroups][64][2];
   const int e = blockIdx.y;
+  // src2 (a bf16 remainder) exists only for experts whose flag is set
+  if (src2_flags && __ldg(src2_flags + e) == 0) src2 = nullptr;
   const int tx = threadIdx.x, g = threadIdx.y;
   const int c = (blockIdx.x * 64 + tx) * 8;
   float acc[8];
@@ -297,6 +300,48 @@ __global__ void __launch_bounds__(64 * kRowGroups) expert_colsum_kernel(
     }
     store8(out + static_cast<int64_t>(e) * C + c, acc);
   }
+}
+
+// Whether each expert's weight gradients need the bf16 remainder (lo) part of
+// their computed operand (dH1 for gate_up, w*a for down).  Without it the
+// operand is rounded to bf16 once, a relative error of up to 2^-8 per value.
+// In a weight-gradient element, a sum over the expert's rows, those errors
+// average out unless a few rows dominate the sum; the routing weight scales
+// every row, so the number of rows that count is the effective row count
+// n_eff = (sum w^2)^2 / sum w^4 over the expert's rows (n_eff = n for equal
+// weights).  Experts with n_eff >= min_neff get flag 0 (one bf16 operand);
+// the rest, and experts without rows, flag 1 (hi + lo).  One warp per
+// expert, fixed summation order.
+__global__ void __launch_bounds__(256) split_select_kernel(
+    const int* __restrict__ offsets, const int* __restrict__ perm,
+    const float* __restrict__ topk_w, int tk, int E, float min_neff, int* __restrict__ lo_flags) {
+  const int lane = threadIdx.x & 31;
+  const int e = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (e >= E) return;
+  const int g0 = __ldg(offsets + e), g1 = min(__ldg(offsets + e + 1), tk);
+  float s2 = 0.f, s4 = 0.f;
+  for (int gi = g0 + lane; gi < g1; gi += 32) {
+    const int slot = __ldg(perm + gi);
+    const float w = (slot >= 0 && slot < tk) ? __ldg(topk_w + slot) : 0.f;
+    const float w2 = w * w;
+    s2 += w2;
+    s4 = fmaf(w2, w2, s4);
+  }
+#pragma unroll
+  for (int d = 16; d > 0; d >>= 1) {
+    s2 += __shfl_xor_sync(0xffffffffu, s2, d);
+    s4 += __shfl_xor_sync(0xffffffffu, s4, d);
+  }
+  // (all-zero weights make the operand exactly zero: no remainder needed;
+  // non-finite weights fail the comparison and keep the remainder)
+  if (lane == 0) lo_flags[e] = (g1 > g0 && s2 * s2 >= min_neff * s4) ? 0 : 1;
+}
+
+cudaError_t launch_split_select(const int* offsets, const int* perm, const float* topk_w, int tk,
+                                int E, float min_neff, int* lo_flags, cudaStream_t st) {
+  split_select_kernel<<<(E + 7) / 8, 256, 0, st>>>(offsets, perm, topk_w, tk, E, min_neff,
+                                                   lo_flags);
+  return cudaGetLastError();
 }
 
 static int grid_for(int64_t rows, int num_sms) {
@@ -392,18 +437,19 @@ cudaError_t launch_bias_slot_dot(const void* dy, const void* b_down, int H, int 
 cudaError_t launch_expert_colsum(const void* src, const void* src2, int C, int64_t ld,
                                  int gather_k, int E, const int* poff, const int* counts,
                                  const int* offsets, const int* perm, const float* topk_w, int tk,
-                                 bool weighted, float* out, int elem_bytes, cudaStream_t st) {
+                                 bool weighted, const int* src2_flags, float* out, int elem_bytes,
+                                 cudaStream_t st) {
   if (C % 8 || E <= 0 || E > 65535) return cudaErrorInvalidValue;
   const dim3 grid((C / 8 + 63) / 64, E), block(64, kRowGroups);
   if (elem_bytes == 2)
     expert_colsum_kernel<<<grid, block, 0, st>>>(
         static_cast<const __nv_bfloat16*>(src), static_cast<const __nv_bfloat16*>(src2), C, ld,
-        gather_k, poff, counts, offsets, perm, topk_w, tk, weighted ? 1 : 0, out);
+        gather_k, poff, counts, offsets, perm, topk_w, tk, weighted ? 1 : 0, src2_flags, out);
   else
     expert_colsum_kernel<<<grid, block, 0, st>>>(static_cast<const float*>(src),
                                                  static_cast<const float*>(src2), C, ld, gather_k,
                                                  poff, counts, offsets, perm, topk_w, tk,
-                                                 weighted ? 1 : 0, out);
+                                                 weighted ? 1 : 0, src2_flags, out);
   return cudaGetLastError();
 }
 

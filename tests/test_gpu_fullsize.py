@@ -106,18 +106,29 @@ def _check_expert_grads(case, run, grads, n_exp, seed, max_rows=4096, hottest=Fa
         assert torch.all(grads[2][int(e)] == 0) and torch.all(grads[3][int(e)] == 0)
 
 
+# Relative agreement of the two gradient sides of <dy, y> (below).  An expert
+# whose weight gradients take w*a as one bf16 value (those with many
+# effectively weighted rows) adds sum_{r,i} x_ri d_ri to <dWd, Wd>, with x_ri =
+# w_r a_ri dA'_ri and d_ri the relative rounding error (|d| <= 2^-8, about
+# uniform): a random-sign sum of standard deviation ~ 2^-8 / sqrt(3) (2.3e-3)
+# of the sum it perturbs, itself of random sign.  1e-2 allows about four
+# standard deviations; with hi + lo operands the sides agree to ~1e-5.
+IDENTITY_REL = 1e-2
+
+
 def _check_identities(case, y, grads):
-    # Both gradient sides equal <dy, y_exact> and carry no bf16 output
-    # rounding, so they must agree closely with each other.  <dy, y> with the
-    # GPU's bf16 y differs from <dy, y_exact> by at most ||dy|| ||y - y_exact||
-    # (Cauchy-Schwarz), i.e. by at most 5e-3 ||dy|| ||y|| under the relative
-    # Frobenius tolerance; <dy, y> itself is a sum of random-sign terms, so a
-    # relative bound on it would be meaningless.
+    # Both gradient sides equal <dy, y_exact> up to the rounding of the
+    # weight gradients' operands (IDENTITY_REL) and carry no bf16 output
+    # rounding.  <dy, y> with the GPU's bf16 y differs from <dy, y_exact> by
+    # at most ||dy|| ||y - y_exact|| (Cauchy-Schwarz), i.e. by at most
+    # 5e-3 ||dy|| ||y|| under the relative Frobenius tolerance; <dy, y> itself
+    # is a sum of random-sign terms, so a relative bound on it would be
+    # meaningless.
     dy, yd = case.dy.double(), y.double()
     ly = float((dy * yd).sum())
     sw = float((case.topk_w.double() * grads[1].double()).sum())
     sd = float((case.w_down.double() * grads[3].double()).sum())
-    assert abs(sw - sd) <= 2e-3 * abs(sd), (sw, sd)
+    assert abs(sw - sd) <= IDENTITY_REL * abs(sd), (sw, sd)
     bound = 5e-3 * float(dy.norm()) * float(yd.norm())
     assert abs(sw - ly) <= bound, (sw, ly, bound)
 
@@ -195,5 +206,5 @@ def test_clamped_glu_workload_with_biases():
     ly = float((dyd * yd).sum())
     sw = float((case.topk_w.double() * grads[1].double()).sum())
     sd = float((case.w_down.double() * grads[3].double()).sum() + (bd.double() * grads[5].double()).sum())
-    assert abs(sw - sd) <= 2e-3 * abs(sd), (sw, sd)
+    assert abs(sw - sd) <= IDENTITY_REL * abs(sd), (sw, sd)
     assert abs(sw - ly) <= 5e-3 * float(dyd.norm()) * float(yd.norm()), (sw, ly)

@@ -278,8 +278,8 @@ def test_expert_counts_at_tile_boundaries(k):
     slots = slots[g.permutation(slots.size)]
     T = slots.size // k
     idx = torch.from_numpy(slots[:T * k].reshape(T, k).astype(np.int32))
-    # fan-in weights: the structure is under test, not a heavy-tailed y (std 0.3 puts
-    # |y| at 8x its rms, where the bf16 output spacing alone exceeds 3e-2 rms)
+    # fan-in weights: the structure is under test here; the heavy-tailed std-0.3
+    # draw of the same counts is the next test
     r = _recipe(T, H, I, E, k, ACT_CLAMPED_GLU, seed=60 + k, routing="uniform_ids")
     case = synth.make_case(r)
     case.topk_idx = idx
@@ -300,6 +300,64 @@ def test_expert_counts_at_tile_boundaries(k):
     assert_dw_close(dtw.cpu().numpy(), ref[1])
     for e in range(E):   # per expert: each boundary case on its own
         if got[e]:
+            assert_close("dw_gate_up[%d]" % e, dwgu[e].cpu().numpy(), ref[2][e])
+            assert_close("dw_down[%d]" % e, dwd[e].cpu().numpy(), ref[3][e])
+        else:
+            assert torch.all(dwgu[e] == 0) and torch.all(dwd[e] == 0)
+
+
+def _bf16_ulp(v):
+    """Spacing of the bf16 values at |v| (2^(e-7) for |v| in [2^e, 2^(e+1)))."""
+    a = np.maximum(np.abs(v), np.finfo(np.float32).tiny)
+    return np.exp2(np.floor(np.log2(a)) - 7)
+
+
+@pytest.mark.parametrize("k", [1, 2])
+def test_expert_counts_at_tile_boundaries_heavy_tailed(k):
+    """The tile-boundary counts with std-0.3 weights, where |y| and |dx| reach
+    7-10x their rms.  The bf16 outputs y and dx then carry two errors at their
+    largest elements: the arithmetic's (chiefly the bf16 rounding of the
+    activation before the down GEMM, ~1e-2 rms at the tails) and their own
+    rounding to bf16, one step of which is 2^-7 of the value, up to 0.055 rms
+    here.  Where the exact value lies near a rounding midpoint, the first
+    error moves the second to the neighbouring bf16 value, so no bf16-output
+    evaluation that is not correctly rounded can promise 3e-2 rms there.  y
+    and dx are held to the relative Frobenius bound and to max abs error
+    <= 3e-2 rms plus one bf16 step of the reference element; the fp32 outputs
+    (d(topk w), every expert's weight gradients) keep the usual bounds."""
+    from dispatch_gemm_combine_gb300 import MOE_BF16
+    from dispatch_gemm_combine_gb300.runner import LayerRunner
+    from tests.helpers import MAX_ABS_RMS, REL_FROB, rel_frob
+    counts = [1, 15, 16, 17, 255, 256, 257, 271, 272, 273, 511, 512, 513, 0, 64, 65]
+    E, H, I = len(counts), 128, 96
+    slots = np.repeat(np.arange(E), counts)
+    g = np.random.default_rng(41 + k)
+    slots = slots[g.permutation(slots.size)]
+    T = slots.size // k
+    idx = torch.from_numpy(slots[:T * k].reshape(T, k).astype(np.int32))
+    r = _recipe(T, H, I, E, k, ACT_CLAMPED_GLU, seed=60 + k, routing="uniform_ids", std=0.3)
+    case = synth.make_case(r)
+    case.topk_idx = idx
+    x, idx_np, w, wgu, wd, dy = oracle_inputs(case)
+    d = to_device(case)
+    run = LayerRunner(T, H, I, E, k, r.act, MOE_BF16, r.limit, r.alpha)
+    run.plan(d.topk_idx)
+    y = run.forward(d.x, d.topk_idx, d.topk_w, d.w_gate_up, d.w_down).clone()
+    dx, dtw, dwgu, dwd = [t.clone() for t in run.backward(d.dy, d.x, d.topk_idx, d.topk_w,
+                                                          d.w_gate_up, d.w_down)]
+    torch.cuda.synchronize()
+    run.check()
+    ref = oracle.moe_backward(dy, x, idx_np, w, wgu, wd, r.act)
+    for name, got, want in (("y", y, oracle.moe_forward(x, idx_np, w, wgu, wd, r.act)),
+                            ("dx", dx, ref[0])):
+        got = got.double().cpu().numpy()
+        rms = float(np.sqrt(np.mean(want ** 2)))
+        assert rel_frob(got, want) <= REL_FROB, name
+        excess = np.abs(got - want) - (MAX_ABS_RMS * rms + _bf16_ulp(want))
+        assert np.all(excess <= 0), (name, float(excess.max()) / rms)
+    assert_dw_close(dtw.cpu().numpy(), ref[1])
+    for e in range(E):
+        if counts[e]:
             assert_close("dw_gate_up[%d]" % e, dwgu[e].cpu().numpy(), ref[2][e])
             assert_close("dw_down[%d]" % e, dwd[e].cpu().numpy(), ref[3][e])
         else:
