@@ -20,7 +20,8 @@ __all__ = [
     "moe_plan", "moe_ffn_fwd", "moe_ffn_bwd", "moe_get_device_error", "moe_status_string",
     "moe_set_wait_timeout_ns", "moe_kernel_launch_count", "moe_profile_enable",
     "moe_profile_read", "moe_profile_kernel_name", "Shape", "alloc_plan", "workspace", "plan", "ffn_fwd", "ffn_bwd",
-    "bias_struct", "check_device_error",
+    "bias_struct", "check_device_error", "moe_gather_rows", "moe_combine_rows", "gather_rows",
+    "combine_rows",
 ]
 
 MOE_OK = 0
@@ -45,7 +46,8 @@ class MoeShape(ctypes.Structure):
     _fields_ = [("T", ctypes.c_int64), ("H", ctypes.c_int32), ("I", ctypes.c_int32),
                 ("E", ctypes.c_int32), ("k", ctypes.c_int32), ("act", ctypes.c_int32),
                 ("clamp_limit", ctypes.c_float), ("alpha", ctypes.c_float),
-                ("dtype", ctypes.c_int32), ("gate_up_layout", ctypes.c_int32)]
+                ("dtype", ctypes.c_int32), ("gate_up_layout", ctypes.c_int32),
+                ("out_fp32", ctypes.c_int32)]
 
 
 class MoePlan(ctypes.Structure):
@@ -108,6 +110,11 @@ def lib():
     L.moe_profile_read.restype = ctypes.c_int
     L.moe_profile_kernel_name.argtypes = [ctypes.c_int]
     L.moe_profile_kernel_name.restype = ctypes.c_char_p
+    L.moe_gather_rows.argtypes = [P, ctypes.c_int64, ctypes.c_int32, P, ctypes.c_int64,
+                                  ctypes.c_int64, P, P]
+    L.moe_gather_rows.restype = ctypes.c_int
+    L.moe_combine_rows.argtypes = [S, P, P, P, ctypes.c_int32, P, P]
+    L.moe_combine_rows.restype = ctypes.c_int
     _lib = L
     return L
 
@@ -176,6 +183,15 @@ def moe_profile_read():
     return {moe_profile_kernel_name(i): (ms[i], cnt[i]) for i in range(min(k, n))}
 
 
+def moe_gather_rows(index, n, div, src, src_rows, row_bytes, dst, stream):
+    return lib().moe_gather_rows(index, n, div, src, src_rows, row_bytes, dst, stream)
+
+
+def moe_combine_rows(shape, inv, topk_w, src, src_fp32, dst, stream):
+    return lib().moe_combine_rows(ctypes.byref(shape), inv, topk_w, src, 1 if src_fp32 else 0,
+                                  dst, stream)
+
+
 def moe_plan_noalloc(shape, topk_idx, plan, stream):
     """moe_plan without a workspace, for callers that cannot allocate device
     memory when they build a plan; its scratch is a fixed array inside the
@@ -189,8 +205,9 @@ def moe_plan_noalloc(shape, topk_idx, plan, stream):
 
 # ---------------------------------------------------------------- torch helpers
 def Shape(T, H, I, E, k, act=MOE_ACT_SWIGLU, dtype=MOE_BF16, clamp_limit=7.0, alpha=1.702,
-          gate_up_layout=0):
-    return MoeShape(T, H, I, E, k, act, clamp_limit, alpha, dtype, gate_up_layout)
+          gate_up_layout=0, out_fp32=0):
+    return MoeShape(T, H, I, E, k, act, clamp_limit, alpha, dtype, gate_up_layout,
+                    1 if out_fp32 else 0)
 
 
 def _ptr(t):
@@ -272,6 +289,28 @@ def ffn_bwd(shape, dy, x, topk_idx, topk_w, w_gate_up, w_down, plan_struct, save
                        _ptr(w_down), bias, plan_struct, _ptr(saved), _ptr(dx), _ptr(d_topk_w),
                        _ptr(dw_gate_up), _ptr(dw_down), _ptr(ws), ws.numel(), _stream(stream)),
            "moe_ffn_bwd")
+
+
+def gather_rows(index, div, src, dst, stream=None):
+    """dst[r] = src[index[r] // div] for every row r of dst (torch tensors on
+    the device; src and dst rows of equal byte size, index int32)."""
+    n = index.numel()
+    row_bytes = dst.element_size() * (dst.numel() // max(1, dst.shape[0])) if dst.dim() else 0
+    if dst.shape[0] != n:
+        raise ValueError("gather_rows: dst has %d rows for %d indices" % (dst.shape[0], n))
+    src_rows = src.shape[0] if src.dim() else 1
+    if n and src.element_size() * (src.numel() // max(1, src_rows)) != row_bytes:
+        raise ValueError("gather_rows: src and dst rows differ in size")
+    _check(moe_gather_rows(_ptr(index), n, div, _ptr(src), src_rows, row_bytes, _ptr(dst),
+                           _stream(stream)), "moe_gather_rows")
+
+
+def combine_rows(shape, inv, src, dst, topk_w=None, stream=None):
+    """dst[t] = sum_j (topk_w[t, j] or 1) * src[inv[t*k + j]] (torch tensors;
+    src fp32 or the storage dtype, dst as shape.out_fp32 says)."""
+    import torch
+    _check(moe_combine_rows(shape, _ptr(inv), _ptr(topk_w), _ptr(src), src.dtype == torch.float32,
+                            _ptr(dst), _stream(stream)), "moe_combine_rows")
 
 
 def check_device_error(ws, stream=None):

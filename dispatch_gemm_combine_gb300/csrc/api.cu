@@ -85,13 +85,13 @@ std::atomic<uint64_t> g_timeout_ns{2000000000ull};
 enum Kind : int {
   kKPlan = 0, kKOffsets, kKGather, kKFwdGateUp, kKFwdDown, kKCombine, kKDgradDown, kKDwReduce,
   kKWgradDown, kKDgradGateUp, kKWgradGateUp, kKMemset, kKTranspose, kKRoute, kKBiasDot,
-  kKBiasGrad, kKSplitSelect, kNumKinds
+  kKBiasGrad, kKSplitSelect, kKGatherIndex, kKCombineDense, kNumKinds
 };
 const char* const kKindNames[kNumKinds] = {
     "plan", "padded_offsets", "gather_rows", "gemm_fwd_gate_up_act", "gemm_fwd_down_scale",
     "combine", "gemm_dgrad_down_act_bwd", "dw_reduce", "gemm_wgrad_down", "gemm_dgrad_gate_up",
     "gemm_wgrad_gate_up", "memset", "transpose_f32", "route", "bias_slot_dot", "bias_colsum",
-    "split_select"};
+    "split_select", "gather_index", "combine_dense"};
 
 std::atomic<uint64_t> g_launches{0};
 std::atomic<int> g_profile{0};
@@ -236,6 +236,7 @@ bool shape_ok(const moe_shape* s) {
   if (s->dtype != MOE_BF16 && s->dtype != MOE_FP32) return false;
   if (s->gate_up_layout != MOE_GATE_UP_CONCAT && s->gate_up_layout != MOE_GATE_UP_INTERLEAVED)
     return false;
+  if (s->out_fp32 != 0 && s->out_fp32 != 1) return false;
   if (s->T * static_cast<int64_t>(s->k) >= (1ll << 31)) return false;
   return true;
 }
@@ -272,6 +273,17 @@ size_t saved_rows(const moe_shape* s) {
 size_t saved_h1_offset(const moe_shape* s) {
   return align256(saved_rows(s) * s->H * elem_bytes(s));
 }
+// The saved pre-activations are fp16 for the clamped GLU with bf16 storage
+// when fp16 represents the clamp limit exactly and |L| <= 32768 (values past
+// the clamp become markers, values inside stay inside, so the backward's
+// clamp masks are exact), fp32 otherwise.
+bool h1_half(const moe_shape* s) {
+  if (elem_bytes(s) != 2 || s->act != MOE_ACT_CLAMPED_GLU) return false;
+  const float L = s->clamp_limit;
+  if (!(L >= -32768.f && L <= 32768.f)) return false;
+  return __half2float(__float2half_rn(L)) == L;
+}
+size_t h1_elem_bytes(const moe_shape* s) { return h1_half(s) ? 2 : 4; }
 
 Layout layout(const moe_shape* s, int which) {
   Layout L;
@@ -322,7 +334,7 @@ Layout layout(const moe_shape* s, int which) {
   }
   if (which == 3) {   // backward without a saved context: recompute it
     L.xp = take(es * R * s->H);
-    L.h1 = take(sizeof(float) * R * 2 * s->I);
+    L.h1 = take(h1_elem_bytes(s) * R * 2 * s->I);
     if (es == 4) L.wguT = take(sizeof(float) * s->E * 2ull * s->I * s->H);
   }
   L.total = off;
@@ -370,6 +382,7 @@ GemmArgs base_args(const moe_shape* s, const int* poff, const int* counts, const
   a.alpha = s->alpha;
   a.I = s->I;
   a.rows_max = rows_max(s);
+  a.h1_half = h1_half(s) ? 1 : 0;
   a.err = err;
   a.timeout_ns = g_timeout_ns.load();
   return a;
@@ -381,7 +394,7 @@ GemmArgs base_args(const moe_shape* s, const int* poff, const int* counts, const
 // weights into wguT.
 moe_status enqueue_gate_up(const moe_shape* s, const void* xp, const void* w_gate_up,
                            const void* b_gate_up, float* wguT,
-                           void* aact, float* h1, int* poff, const int* counts,
+                           void* aact, void* h1, int* poff, const int* counts,
                            const int* offsets, const int* perm, const float* topk_w, int* err,
                            int sms, cudaStream_t st) {
   const int es = elem_bytes(s);
@@ -420,7 +433,7 @@ moe_status enqueue_gate_up(const moe_shape* s, const void* xp, const void* w_gat
   a1.out[0] = out_view(aact, I, R, I);
   if (h1) {
     a1.out[1] = out_view(h1, 2ll * I, R, I);
-    a1.out[2] = out_view(h1 + I, 2ll * I, R, I);
+    a1.out[2] = out_view(static_cast<char*>(h1) + h1_elem_bytes(s) * I, 2ll * I, R, I);
   }
   a1.num_kb = (H + BK - 1) / BK;
   a1.n_tiles = (I + gemm_block_n(kFwdGateUp, es) - 1) / gemm_block_n(kFwdGateUp, es);
@@ -463,7 +476,7 @@ size_t moe_workspace_size(const moe_shape* shape, int which) {
 
 size_t moe_saved_size(const moe_shape* shape) {
   if (!shape_ok(shape)) return 0;
-  return saved_h1_offset(shape) + saved_rows(shape) * 2 * shape->I * sizeof(float);
+  return saved_h1_offset(shape) + saved_rows(shape) * 2 * shape->I * h1_elem_bytes(shape);
 }
 
 uint64_t moe_set_wait_timeout_ns(uint64_t ns) { return g_timeout_ns.exchange(ns); }
@@ -612,8 +625,8 @@ moe_status moe_ffn_fwd(const moe_shape* s, const void* x, const int32_t* topk_id
   // backward reads instead of gathering x again
   void* xp = saved ? saved : at<char>(ws, L.xp);
   void* aact = at<char>(ws, L.act);
-  float* h1_saved = saved ? reinterpret_cast<float*>(static_cast<char*>(saved) + saved_h1_offset(s))
-                          : nullptr;
+  void* h1_saved = saved ? static_cast<void*>(static_cast<char*>(saved) + saved_h1_offset(s))
+                         : nullptr;
   MOE_CUDA(tracked(kKGather, 1, st, [&] {
     return launch_gather_rows(x, H, s->k, E, poff, counts, offsets, perm, static_cast<int>(Tk),
                               R, xp, es, sms, st);
@@ -653,9 +666,11 @@ moe_status moe_ffn_fwd(const moe_shape* s, const void* x, const int32_t* topk_id
   a2.n_tiles = (H + gemm_block_n(kFwdDown, es) - 1) / gemm_block_n(kFwdDown, es);
   MOE_CUDA(tracked(kKFwdDown, 1, st, [&] { return launch_gemm(kFwdDown, es, m2, a2, sms, st); }));
 
-  // combine
+  // combine (y in the storage dtype, or fp32 on request)
+  const int y_bytes = s->out_fp32 ? 4 : es;
   MOE_CUDA(tracked(kKCombine, 1, st, [&] {
-    return launch_combine(ow, H, s->k, E, topk_idx, inv, offsets, poff, s->T, R, y, es, sms, st);
+    return launch_combine(ow, H, s->k, E, topk_idx, inv, offsets, poff, s->T, R, y, y_bytes, sms,
+                          st);
   }));
   return MOE_OK;
 }
@@ -724,13 +739,13 @@ moe_status moe_ffn_bwd(const moe_shape* s, const void* dy, const void* x, const 
   }
 
   void* dyp = at<char>(ws, L.dyp);
-  // the forward's expert-grouped x rows and fp32 pre-activations: saved, or
+  // the forward's expert-grouped x rows and pre-activations: saved, or
   // recomputed here by the forward's gather and gate_up GEMM (bit-identical)
   void* xp = recompute ? at<char>(ws, L.xp) : const_cast<void*>(saved);
-  const float* h1_saved =
-      recompute ? at<float>(ws, L.h1)
-                : reinterpret_cast<const float*>(static_cast<const char*>(saved) +
-                                                 saved_h1_offset(s));
+  const void* h1_saved =
+      recompute ? static_cast<const void*>(at<char>(ws, L.h1))
+                : static_cast<const void*>(static_cast<const char*>(saved) +
+                                           saved_h1_offset(s));
   void* dh1 = at<char>(ws, L.dh1);
   void* aw = at<char>(ws, L.aw);
   const bool split = (es == 2);
@@ -750,7 +765,7 @@ moe_status moe_ffn_bwd(const moe_shape* s, const void* dy, const void* x, const 
     // the down dgrad overwrites
     const moe_status gs =
         enqueue_gate_up(s, xp, w_gate_up, bias.b_gate_up, es == 4 ? at<float>(ws, L.wguT) : nullptr,
-                        dh1, const_cast<float*>(h1_saved), poff, counts, offsets, perm, topk_w,
+                        dh1, const_cast<void*>(h1_saved), poff, counts, offsets, perm, topk_w,
                         err, sms, st);
     if (gs != MOE_OK) return gs;
   }
@@ -874,7 +889,8 @@ moe_status moe_ffn_bwd(const moe_shape* s, const void* dy, const void* x, const 
   a3.n_tiles = (H + gemm_block_n(kDgradGateUp, es) - 1) / gemm_block_n(kDgradGateUp, es);
   MOE_CUDA(tracked(kKDgradGateUp, 1, st, [&] { return launch_gemm(kDgradGateUp, es, m3, a3, sms, st); }));
   MOE_CUDA(tracked(kKCombine, 1, st, [&] {
-    return launch_combine(dxp, H, s->k, E, topk_idx, inv, offsets, poff, s->T, R, dx, es, sms, st);
+    return launch_combine(dxp, H, s->k, E, topk_idx, inv, offsets, poff, s->T, R, dx,
+                          s->out_fp32 ? 4 : es, sms, st);
   }));
 
   // (4) gate_up wgrad: dWgu[e] = Xp_e^T dH1_e  (dH1 as a bf16 hi/lo pair)
@@ -907,6 +923,40 @@ moe_status moe_ffn_bwd(const moe_shape* s, const void* dy, const void* x, const 
   a4.m_tiles = (H + gemm_block_m(kWgradGateUp, es) - 1) / gemm_block_m(kWgradGateUp, es);
   a4.n_tiles = (2 * I + bn4 - 1) / bn4;
   MOE_CUDA(tracked(kKWgradGateUp, 1, st, [&] { return launch_gemm(kWgradGateUp, es, m4, a4, sms, st); }));
+  return MOE_OK;
+}
+
+moe_status moe_gather_rows(const int32_t* index, int64_t n, int32_t div, const void* src,
+                           int64_t src_rows, int64_t row_bytes, void* dst, moe_stream_t stream) {
+  if (n < 0 || div < 1 || row_bytes <= 0 || (row_bytes % 4) || src_rows < 0 ||
+      row_bytes / 4 > (1ll << 30))
+    return MOE_ERR_INVALID_ARG;
+  if (n == 0) return MOE_OK;
+  if (!index || !dst || (!src && src_rows > 0)) return MOE_ERR_INVALID_ARG;
+  int sms = 0;
+  const moe_status ds = device_info(&sms);
+  if (ds != MOE_OK) return ds;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  MOE_CUDA(tracked(kKGatherIndex, 1, st, [&] {
+    return launch_gather_index(index, n, div, src, src_rows, row_bytes, dst, sms, st);
+  }));
+  return MOE_OK;
+}
+
+moe_status moe_combine_rows(const moe_shape* s, const int32_t* inv, const float* topk_w,
+                            const void* src, int32_t src_fp32, void* dst, moe_stream_t stream) {
+  if (!shape_ok(s) || (src_fp32 != 0 && src_fp32 != 1)) return MOE_ERR_INVALID_ARG;
+  if (s->T == 0) return MOE_OK;
+  if (!inv || !src || !dst || !aligned16(src) || !aligned16(dst)) return MOE_ERR_INVALID_ARG;
+  int sms = 0;
+  const moe_status ds = device_info(&sms);
+  if (ds != MOE_OK) return ds;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const int es = elem_bytes(s);
+  MOE_CUDA(tracked(kKCombineDense, 1, st, [&] {
+    return launch_combine_dense(src, src_fp32 ? 4 : es, s->H, s->k, inv, topk_w, s->T, dst,
+                                s->out_fp32 ? 4 : es, sms, st);
+  }));
   return MOE_OK;
 }
 

@@ -281,6 +281,21 @@ __device__ __forceinline__ void act_bwd2(float2 g, float2 u, float L, float alph
   }
 }
 
+// Two fp32 values as one 32-bit pair of the 16-bit output type (round to
+// nearest).
+template <typename O>
+__device__ __forceinline__ uint32_t pack2(float a, float b);
+template <>
+__device__ __forceinline__ uint32_t pack2<__nv_bfloat16>(float a, float b) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+template <>
+__device__ __forceinline__ uint32_t pack2<__half>(float a, float b) {
+  const __half2 h = __floats2half2_rn(a, b);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
 // Store this warp's 32x32 output tile: lane i holds row r0+i, columns
 // [c0, c0+32).  The tile goes through a per-warp shared-memory transpose
 // (rows padded so that both the row-wise writes and the column-wise reads
@@ -315,10 +330,9 @@ __device__ __forceinline__ void store_tile(const OutDesc& o, int b, int r0, int 
     __nv_bfloat16* row = st + lane * 40;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      uint4 pk;
-      __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&pk);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) h[i] = __floats2bfloat162_rn(v[8 * j + 2 * i], v[8 * j + 2 * i + 1]);
+      const uint4 pk = make_uint4(pack2<O>(v[8 * j], v[8 * j + 1]), pack2<O>(v[8 * j + 2], v[8 * j + 3]),
+                                  pack2<O>(v[8 * j + 4], v[8 * j + 5]),
+                                  pack2<O>(v[8 * j + 6], v[8 * j + 7]));
       *reinterpret_cast<uint4*>(row + 8 * j) = pk;
     }
     __syncwarp();
@@ -416,6 +430,23 @@ __device__ __forceinline__ float bf16_round(float x) {
 __device__ __forceinline__ void split_bf16(float x, float& hi, float& lo) {
   hi = bf16_round(x);
   lo = x - hi;
+}
+
+// The clamped GLU's saved pre-activations may be fp16 (bf16 storage, a clamp
+// limit L that fp16 represents exactly, |L| <= 32768; the host decides):
+// the backward needs gc = min(g, L), uc = clamp(u, -L, L) and the masks
+// [g <= L], [-L <= u <= L].  A value past its clamp is kept as an infinite
+// marker (it decodes to the clamp with mask 0); a value inside rounds to the
+// nearest fp16 value, which stays inside because L is an fp16 value, so
+// every mask is exact.  g below -65504 is kept as -65504: the activation and
+// its derivatives there are the fp32 results at any such g (sigmoid(alpha g)
+// underflows to 0 for alpha >= 0.002).  NaN stays NaN.  The fp16 store does
+// the rounding.
+__device__ __forceinline__ float h1_code_gate(float g, float L) {
+  return g > L ? __int_as_float(0x7f800000) : (g < -65504.f ? -65504.f : g);
+}
+__device__ __forceinline__ float h1_code_up(float u, float L) {
+  return u > L ? __int_as_float(0x7f800000) : (u < -L ? __int_as_float(0xff800000) : u);
 }
 
 // Add the bias values p[0, N) of a column chunk to v: every lane of the warp
@@ -950,8 +981,20 @@ __global__ void __launch_bounds__(192, 1)
                 }
               }
               if (args.save_h1) {
-                store_tile<float>(args.out[1], 0, orow, ti.n0 + c * 32, v, my_epi, lane);
-                store_tile<float>(args.out[2], 0, orow, ti.n0 + c * 32, u, my_epi, lane);
+                if (ACT == 1 && !C::kTf32 && args.h1_half) {
+                  // fp16 context (see h1_code_gate)
+                  float gq[32], uq[32];
+#pragma unroll
+                  for (int i = 0; i < 32; ++i) {
+                    gq[i] = h1_code_gate(v[i], args.limit);
+                    uq[i] = h1_code_up(u[i], args.limit);
+                  }
+                  store_tile<__half>(args.out[1], 0, orow, ti.n0 + c * 32, gq, my_epi, lane);
+                  store_tile<__half>(args.out[2], 0, orow, ti.n0 + c * 32, uq, my_epi, lane);
+                } else {
+                  store_tile<float>(args.out[1], 0, orow, ti.n0 + c * 32, v, my_epi, lane);
+                  store_tile<float>(args.out[2], 0, orow, ti.n0 + c * 32, u, my_epi, lane);
+                }
               }
 #pragma unroll
               for (int i = 0; i < 32; ++i) {
@@ -993,41 +1036,73 @@ __global__ void __launch_bounds__(192, 1)
                                 *reinterpret_cast<const float(*)[32]>(w2 + 32), my_epi, lane);
             }
           } else {  // kDgradDown
-            // saved fp32 pre-activations of this row: gate at [0, I), up at [I, 2I);
-            // each lane copies its own row's 32 gate + 32 up values of a column
-            // chunk into shared memory with cp.async, one chunk ahead
-            const float* h1row = static_cast<const float*>(args.h1) + static_cast<int64_t>(row) * 2 * args.I;
+            // saved pre-activations of this row, gate at [0, I), up at [I, 2I):
+            // fp32, or fp16 (h1_half, see h1_code_gate).  Each lane copies its own row's 32 gate + 32 up
+            // values of a column chunk into shared memory with cp.async, one
+            // chunk ahead.
+            const int64_t h1off = static_cast<int64_t>(row) * 2 * args.I;   // elements
             const float* h1s = reinterpret_cast<const float*>(my_h1) + lane * 68;
             const uint32_t h1s_s = smem_u32(my_h1) + lane * 68 * 4;
-            auto prefetch = [&](int c) {
-              const int i0 = ti.n0 + c * 32;
-#pragma unroll
-              for (int j = 0; j < 8; ++j) {
-                const int col = i0 + 4 * j;
-                const bool in = col < args.I;   // I % 8 == 0: 16-byte units are all in or all out
-                cp_async16(h1s_s + j * 16, in ? h1row + col : h1row, in ? 16u : 0u);
-                cp_async16(h1s_s + 128 + j * 16, in ? h1row + args.I + col : h1row, in ? 16u : 0u);
-              }
-              cp_async_commit();
-            };
             // column chunks that hold outputs (fewer in the ragged last tile)
             const int nch = min(BN / 32, (args.I - ti.n0 + 31) / 32);
-            prefetch(0);
             float dot = 0.f;
             auto run = [&](auto act_c) {
             constexpr int ACT = decltype(act_c)::value;
+            // fp16 context: the clamped GLU only (the host sets h1_half)
+            const bool half = (ACT == 1 && !C::kTf32 && args.h1_half);
+            // I % 8 == 0: 16-byte units are all inside the row or all past it
+            auto prefetch = [&](int c) {
+              const int i0 = ti.n0 + c * 32;
+              if (half) {
+                const __half* h1row = static_cast<const __half*>(args.h1) + h1off;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                  const int col = i0 + 8 * j;
+                  const bool in = col < args.I;
+                  cp_async16(h1s_s + j * 16, in ? h1row + col : h1row, in ? 16u : 0u);
+                  cp_async16(h1s_s + 64 + j * 16, in ? h1row + args.I + col : h1row, in ? 16u : 0u);
+                }
+              } else {
+                const float* h1row = static_cast<const float*>(args.h1) + h1off;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                  const int col = i0 + 4 * j;
+                  const bool in = col < args.I;
+                  cp_async16(h1s_s + j * 16, in ? h1row + col : h1row, in ? 16u : 0u);
+                  cp_async16(h1s_s + 128 + j * 16, in ? h1row + args.I + col : h1row, in ? 16u : 0u);
+                }
+              }
+              cp_async_commit();
+            };
+            prefetch(0);
 #pragma unroll 1
             for (int c = 0; c < nch; ++c) {
               tmem_ld32(tacc + c * 32, v);   // dA' (before the routing weight)
               const int i0 = ti.n0 + c * 32;
               float g[32], u[32];
               cp_async_wait_all();
+              if (half) {
+                const uint4* hs = reinterpret_cast<const uint4*>(h1s);
 #pragma unroll
-              for (int j = 0; j < 8; ++j) {
-                const float4 gv = *reinterpret_cast<const float4*>(h1s + 4 * j);
-                const float4 uv = *reinterpret_cast<const float4*>(h1s + 32 + 4 * j);
-                g[4 * j] = gv.x; g[4 * j + 1] = gv.y; g[4 * j + 2] = gv.z; g[4 * j + 3] = gv.w;
-                u[4 * j] = uv.x; u[4 * j + 1] = uv.y; u[4 * j + 2] = uv.z; u[4 * j + 3] = uv.w;
+                for (int j = 0; j < 4; ++j) {
+                  const uint4 gv = hs[j], uv = hs[4 + j];
+                  const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w}, uw[4] = {uv.x, uv.y, uv.z, uv.w};
+#pragma unroll
+                  for (int i = 0; i < 4; ++i) {
+                    const float2 gf = __half22float2(*reinterpret_cast<const __half2*>(&gw[i]));
+                    const float2 uf = __half22float2(*reinterpret_cast<const __half2*>(&uw[i]));
+                    g[8 * j + 2 * i] = gf.x; g[8 * j + 2 * i + 1] = gf.y;
+                    u[8 * j + 2 * i] = uf.x; u[8 * j + 2 * i + 1] = uf.y;
+                  }
+                }
+              } else {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                  const float4 gv = *reinterpret_cast<const float4*>(h1s + 4 * j);
+                  const float4 uv = *reinterpret_cast<const float4*>(h1s + 32 + 4 * j);
+                  g[4 * j] = gv.x; g[4 * j + 1] = gv.y; g[4 * j + 2] = gv.z; g[4 * j + 3] = gv.w;
+                  u[4 * j] = uv.x; u[4 * j + 1] = uv.y; u[4 * j + 2] = uv.z; u[4 * j + 3] = uv.w;
+                }
               }
               // refill the staging row with the next chunk as early as possible:
               // a use of every value read above orders those reads before the

@@ -71,6 +71,18 @@ cudaError_t launch_expert_colsum(const void* src, const void* src2, int C, int64
 cudaError_t launch_split_select(const int* offsets, const int* perm, const float* topk_w, int tk,
                                 int E, float min_neff, int* lo_flags, cudaStream_t st);
 
+// ---- dense row movement of the expert-parallel exchange (permute.cu)
+// dst[r] = src[index[r] / div] for r < n (rows of row_bytes bytes, a multiple
+// of 4); an index outside [0, src_rows * div) gives a zero row.
+cudaError_t launch_gather_index(const int* index, int64_t n, int div, const void* src,
+                                int64_t src_rows, int64_t row_bytes, void* dst, int num_sms,
+                                cudaStream_t st);
+// dst[t] = sum_{j<k} (w[t*k+j] or 1) src[inv[t*k+j]] in fp32, j ascending;
+// src / dst elements of 2 (bf16) or 4 (fp32) bytes; H % 8 == 0.
+cudaError_t launch_combine_dense(const void* src, int src_bytes, int H, int k, const int* inv,
+                                 const float* w, int64_t T, void* dst, int dst_bytes, int num_sms,
+                                 cudaStream_t st);
+
 // ---- grouped tensor-core GEMMs (gemm_*.cu)
 enum GemmMode : int {
   kFwdGateUp = 0,    // A_act = act(Xp Wgu[e]) (+ saved pre-activations)
@@ -107,6 +119,7 @@ struct GemmArgs {
   float limit;
   float alpha;
   int save_h1;          // kFwdGateUp: also store the gate / up pre-activations
+  int h1_half;          // clamped GLU, bf16: the saved pre-activations are fp16 (else fp32)
   const void* bias;     // kFwdGateUp: b_gate_up [E, 2I]; kFwdDown: b_down [E, H]; or null
   const void* h1;       // kDgradDown: saved pre-activations [rows_max, 2I]
   int I;

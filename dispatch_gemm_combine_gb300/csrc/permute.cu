@@ -12,6 +12,8 @@
 // All are HBM-bound and use 16-byte vector accesses.  The row kernels run one
 // warp per row on a grid sized as a multiple of the SM count; the column sums
 // run one thread per 8 columns of one expert.
+#include <algorithm>
+
 #include "kernels.h"
 
 namespace moe {
@@ -341,6 +343,100 @@ cudaError_t launch_split_select(const int* offsets, const int* perm, const float
                                 int E, float min_neff, int* lo_flags, cudaStream_t st) {
   split_select_kernel<<<(E + 7) / 8, 256, 0, st>>>(offsets, perm, topk_w, tk, E, min_neff,
                                                    lo_flags);
+  return cudaGetLastError();
+}
+
+// ---- dense row movement for the expert-parallel exchange ----------------
+// dst[r] = src[index[r] / div] for r < n, rows of row_bytes bytes (a multiple
+// of 4; 16-byte accesses when rows and pointers allow).  An index outside
+// [0, src_rows * div) gives a zero row.  One warp per row.
+template <typename V>
+__global__ void __launch_bounds__(256) gather_index_kernel(const int* __restrict__ index, int64_t n,
+                                                           int div, const V* __restrict__ src,
+                                                           int64_t src_rows, int vec_per_row,
+                                                           V* __restrict__ dst) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+  for (int64_t r = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); r < n;
+       r += warps) {
+    const int i = __ldg(index + r);
+    const int64_t sr = (i >= 0) ? static_cast<int64_t>(i) / div : -1;
+    V* d = dst + r * vec_per_row;
+    if (sr < 0 || sr >= src_rows) {
+      V z;
+      memset(&z, 0, sizeof(V));
+      for (int c = lane; c < vec_per_row; c += 32) d[c] = z;
+    } else {
+      const V* sp = src + sr * vec_per_row;
+      for (int c = lane; c < vec_per_row; c += 32) d[c] = __ldg(sp + c);
+    }
+  }
+}
+
+// dst[t] = sum_{j < k} (w[t*k+j] or 1) * src[inv[t*k+j]] in fp32, j ascending,
+// rows of H elements (H % 8 == 0); a slot whose inv is outside [0, T*k)
+// contributes nothing.  One warp per token, 8 elements per lane and step.
+template <typename Tin, typename Tout>
+__global__ void __launch_bounds__(256) combine_dense_kernel(const Tin* __restrict__ src, int H,
+                                                            int k, const int* __restrict__ inv,
+                                                            const float* __restrict__ w,
+                                                            int64_t T, Tout* __restrict__ dst) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+  const int64_t tk = T * k;
+  for (int64_t t = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); t < T;
+       t += warps) {
+    for (int c = lane * 8; c < H; c += 256) {
+      float acc[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+      for (int j = 0; j < k; ++j) {
+        const int64_t s = t * k + j;
+        const int r = __ldg(inv + s);
+        if (r < 0 || r >= tk) continue;
+        const float sc = w ? __ldg(w + s) : 1.f;
+        float a[8];
+        load8(src + static_cast<int64_t>(r) * H + c, a);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] = fmaf(sc, a[i], acc[i]);
+      }
+      store8(dst + t * H + c, acc);
+    }
+  }
+}
+
+cudaError_t launch_gather_index(const int* index, int64_t n, int div, const void* src,
+                                int64_t src_rows, int64_t row_bytes, void* dst, int num_sms,
+                                cudaStream_t st) {
+  if (n <= 0) return cudaSuccess;
+  const int64_t g = std::min<int64_t>((n + 7) / 8, static_cast<int64_t>(num_sms) * 16);
+  const bool v16 = (row_bytes % 16 == 0) && (reinterpret_cast<uintptr_t>(src) % 16 == 0) &&
+                   (reinterpret_cast<uintptr_t>(dst) % 16 == 0);
+  if (v16)
+    gather_index_kernel<<<static_cast<int>(g), 256, 0, st>>>(
+        index, n, div, static_cast<const uint4*>(src), src_rows, static_cast<int>(row_bytes / 16),
+        static_cast<uint4*>(dst));
+  else
+    gather_index_kernel<<<static_cast<int>(g), 256, 0, st>>>(
+        index, n, div, static_cast<const uint32_t*>(src), src_rows,
+        static_cast<int>(row_bytes / 4), static_cast<uint32_t*>(dst));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_combine_dense(const void* src, int src_bytes, int H, int k, const int* inv,
+                                 const float* w, int64_t T, void* dst, int dst_bytes, int num_sms,
+                                 cudaStream_t st) {
+  if (T <= 0) return cudaSuccess;
+  const int g = static_cast<int>(std::min<int64_t>((T + 7) / 8, static_cast<int64_t>(num_sms) * 16));
+  using B = __nv_bfloat16;
+  if (src_bytes == 2 && dst_bytes == 2)
+    combine_dense_kernel<<<g, 256, 0, st>>>(static_cast<const B*>(src), H, k, inv, w, T, static_cast<B*>(dst));
+  else if (src_bytes == 2)
+    combine_dense_kernel<<<g, 256, 0, st>>>(static_cast<const B*>(src), H, k, inv, w, T, static_cast<float*>(dst));
+  else if (dst_bytes == 2)
+    combine_dense_kernel<<<g, 256, 0, st>>>(static_cast<const float*>(src), H, k, inv, w, T, static_cast<B*>(dst));
+  else
+    combine_dense_kernel<<<g, 256, 0, st>>>(static_cast<const float*>(src), H, k, inv, w, T, static_cast<float*>(dst));
   return cudaGetLastError();
 }
 

@@ -16,19 +16,21 @@ _TORCH_DTYPE = {MOE_BF16: torch.bfloat16, MOE_FP32: torch.float32}
 
 class LayerRunner:
     def __init__(self, T, H, I, E, k, act, dtype=MOE_BF16, clamp_limit=7.0, alpha=1.702,
-                 device="cuda", training=True, backward=True, gate_up_layout=0):
-        self.shape = Shape(T, H, I, E, k, act, dtype, clamp_limit, alpha, gate_up_layout)
+                 device="cuda", training=True, backward=True, gate_up_layout=0, out_fp32=False):
+        """out_fp32: y and dx in fp32 instead of the storage dtype."""
+        self.shape = Shape(T, H, I, E, k, act, dtype, clamp_limit, alpha, gate_up_layout, out_fp32)
         self.device = device
         self.tdtype = _TORCH_DTYPE[dtype]
+        odt = torch.float32 if out_fp32 else self.tdtype
         self.plan_t, self.plan_s = alloc_plan(self.shape, device)
         self.ws_plan = workspace(self.shape, 0, device)
         self.ws_fwd = workspace(self.shape, 1, device)
         self.ws_bwd = workspace(self.shape, 2, device) if backward else None
         self.saved = (torch.empty(moe_saved_size(self.shape), dtype=torch.uint8, device=device)
                       if training else None)
-        self.y = torch.empty((T, H), dtype=self.tdtype, device=device)
+        self.y = torch.empty((T, H), dtype=odt, device=device)
         if backward:
-            self.dx = torch.empty((T, H), dtype=self.tdtype, device=device)
+            self.dx = torch.empty((T, H), dtype=odt, device=device)
             self.d_topk_w = torch.empty((T, k), dtype=torch.float32, device=device)
             self.dw_gate_up = torch.empty((E, H, 2 * I), dtype=torch.float32, device=device)
             self.dw_down = torch.empty((E, I, H), dtype=torch.float32, device=device)

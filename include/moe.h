@@ -86,6 +86,10 @@ typedef struct {
   float alpha;
   int32_t dtype;        /* moe_dtype */
   int32_t gate_up_layout;   /* moe_gate_up_layout */
+  int32_t out_fp32;     /* 0: y and dx in the storage dtype; 1: in fp32 (for
+                         * callers that sum them further, e.g. the combine of
+                         * the expert-parallel exchange, so the rows are not
+                         * rounded twice) */
 } moe_shape;
 
 /* Dispatch plan ("masked indexing" / "sparse token extraction" in the pages'
@@ -136,8 +140,12 @@ size_t moe_workspace_size(const moe_shape* shape, int which);
 /* Bytes of the context the training forward saves for the backward, in the
  * library's expert-grouped, tile-padded row order: the gathered token rows
  * (storage dtype, so the backward does not gather x again), then, 256-byte
- * aligned, the gate_up pre-activations in fp32 (whatever the dtype, so the
- * backward sees the accumulator values, not a bf16 rounding of them).
+ * aligned, the gate_up pre-activations.  Those are fp32 (the accumulator
+ * values, not a bf16 rounding of them), except for the clamped GLU with bf16
+ * storage and a clamp limit that fp16 represents exactly (|L| <= 32768, e.g.
+ * 7.0): there they are fp16 (11 significant bits), values past the clamp are
+ * kept as infinite markers and values inside round to fp16 values inside,
+ * so the clamp masks of the backward are exact.
  * Returns 0 for an invalid shape. */
 size_t moe_saved_size(const moe_shape* shape);
 
@@ -206,6 +214,43 @@ moe_status moe_ffn_bwd(const moe_shape* shape, const void* dy, const void* x,
                        void* dx, float* d_topk_w, float* dw_gate_up,
                        float* dw_down, void* ws, size_t ws_bytes,
                        moe_stream_t stream);
+
+/* ---- expert-parallel exchange primitives ("MoE expert parallel execution
+ * backward", title: experts spread over devices).  A rank that owns a
+ * contiguous range of experts receives, from every rank, the rows of its
+ * experts: the plan's expert-grouped order makes each destination's rows one
+ * contiguous segment, so the dispatch is one gather into that order and one
+ * all-to-all of the segments (by the caller's communication library), and
+ * the combine is the mirrored all-to-all followed by moe_combine_rows.  Both
+ * calls are plain device kernels on `stream`; neither allocates. ---- */
+
+/* Row gather: dst[r] = src[index[r] / div] for r < n.
+ *   index [n] int32 (device); div >= 1: with index = plan->perm, div = k
+ *     gathers token rows into the expert-grouped order (dispatch of x or dy),
+ *     div = 1 gathers per-slot values (routing weights); with index =
+ *     plan->inv, div = 1 brings per-row values back to slot order.
+ *   src [src_rows, row_bytes] and dst [n, row_bytes]: row-major device
+ *     arrays; row_bytes > 0 and a multiple of 4 (16-byte accesses when it is
+ *     a multiple of 16 and both pointers are 16-byte aligned).
+ * An index outside [0, src_rows * div) yields a zero row (no fault, no
+ * error).  n = 0 is a no-op.  Returns MOE_ERR_INVALID_ARG for null pointers
+ * (with n > 0), div < 1 or a bad row_bytes. */
+moe_status moe_gather_rows(const int32_t* index, int64_t n, int32_t div, const void* src,
+                           int64_t src_rows, int64_t row_bytes, void* dst,
+                           moe_stream_t stream);
+
+/* Combine of rows in the plan's dense expert-grouped order back to tokens:
+ *   dst[t] = sum_{j=0..k-1} (topk_w ? topk_w[t,j] : 1) * src[inv[t*k + j]],
+ * summed in fp32 in the order j = 0..k-1 (no atomics; bitwise
+ * reproducible).  shape gives T, H, k, the storage dtype and out_fp32.
+ *   inv [T*k] int32: plan->inv of the plan that ordered the rows.
+ *   src [T*k, H]: fp32 when src_fp32, else the storage dtype.
+ *   dst [T, H]: fp32 when shape->out_fp32, else the storage dtype.
+ * A slot whose inv lies outside [0, T*k) contributes nothing.  16-byte
+ * aligned src and dst; T = 0 is a no-op. */
+moe_status moe_combine_rows(const moe_shape* shape, const int32_t* inv, const float* topk_w,
+                            const void* src, int32_t src_fp32, void* dst,
+                            moe_stream_t stream);
 
 /* Synchronise `stream`, return the first device-side error recorded in the
  * workspace since the last call (MOE_OK if none) and clear it. */

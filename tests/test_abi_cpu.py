@@ -41,17 +41,27 @@ def test_workspace_sizes(L):
     bwd = L.moe_workspace_size(s, 2)
     assert fwd >= rows * (2880 + 2880) * 2
     assert bwd >= rows * (2880 * 2 + 2 * 2880 + 2880) * 2
-    # saved: the grouped bf16 x rows, then the fp32 gate | up pre-activations
-    assert L.moe_saved_size(s) == rows * 2880 * 2 + rows * 2 * 2880 * 4
+    # saved: the grouped bf16 x rows, then the gate | up pre-activations,
+    # fp16 for the clamped GLU with bf16 storage
+    assert L.moe_saved_size(s) == rows * 2880 * 2 + rows * 2 * 2880 * 2
     assert L.moe_workspace_size(s, 0) < fwd
     # a backward without the saved context also holds the grouped x rows and
-    # the fp32 pre-activations it recomputes
-    assert L.moe_workspace_size(s, 3) >= bwd + rows * 2880 * 2 + rows * 2 * 2880 * 4
+    # the pre-activations it recomputes
+    assert L.moe_workspace_size(s, 3) >= bwd + rows * 2880 * 2 + rows * 2 * 2880 * 2
     assert L.moe_workspace_size(s, 4) == 0
-    # few tokens: at most Tk experts hold a row
+    # few tokens: at most Tk experts hold a row; SwiGLU saves fp32
     s2 = L.Shape(3, 64, 64, 256, 2)
     rows2 = (6 + 6 * 127) // 128 * 128
     assert L.moe_saved_size(s2) == rows2 * 64 * 2 + rows2 * 2 * 64 * 4
+    # fp32 storage saves fp32 pre-activations for either activation
+    s3 = L.Shape(3, 64, 64, 256, 2, L.MOE_ACT_CLAMPED_GLU, L.MOE_FP32)
+    assert L.moe_saved_size(s3) == rows2 * 64 * 4 + rows2 * 2 * 64 * 4
+    # fp16 only for a clamp limit that fp16 represents exactly (|L| <= 32768)
+    for lim in (40000.0, 7.3):
+        assert L.moe_saved_size(L.Shape(3, 64, 64, 256, 2, L.MOE_ACT_CLAMPED_GLU,
+                                        clamp_limit=lim)) == rows2 * 64 * 2 + rows2 * 2 * 64 * 4
+    assert L.moe_saved_size(L.Shape(3, 64, 64, 256, 2, L.MOE_ACT_CLAMPED_GLU,
+                                    clamp_limit=10.0)) == rows2 * 64 * 2 + rows2 * 2 * 64 * 2
 
 
 @pytest.mark.parametrize("bad", [dict(H=100), dict(I=12), dict(k=0), dict(E=2, k=3),

@@ -362,3 +362,35 @@ def test_expert_counts_at_tile_boundaries_heavy_tailed(k):
             assert_close("dw_down[%d]" % e, dwd[e].cpu().numpy(), ref[3][e])
         else:
             assert torch.all(dwgu[e] == 0) and torch.all(dwd[e] == 0)
+
+
+@pytest.mark.parametrize("limit", [3.0, 5.3])
+def test_clamped_glu_limits_and_saved_context(limit):
+    """The clamped GLU at other limits: 3.0, an fp16 value (the saved
+    pre-activations are fp16, many of them past the clamp and kept as
+    markers), and 5.3, which fp16 does not represent (fp32 context).  Both
+    against the oracle at the same limit, the recompute backward bit for bit."""
+    from dispatch_gemm_combine_gb300 import MOE_BF16
+    from dispatch_gemm_combine_gb300.runner import LayerRunner
+    r = Recipe("lim", T=400, H=192, I=136, E=6, k=3, act=ACT_CLAMPED_GLU, weight_std=0.2,
+               routing="softmax_topk_renorm", seed=88, limit=limit)
+    case = synth.make_case(r)
+    x, idx, w, wgu, wd, dy = oracle_inputs(case)
+    d = to_device(case)
+    run = LayerRunner(r.T, r.H, r.I, r.E, r.k, r.act, MOE_BF16, limit, r.alpha)
+    run.plan(d.topk_idx)
+    y = run.forward(d.x, d.topk_idx, d.topk_w, d.w_gate_up, d.w_down).clone()
+    grads = [t.clone() for t in run.backward(d.dy, d.x, d.topk_idx, d.topk_w, d.w_gate_up,
+                                             d.w_down)]
+    again = run.backward(d.dy, d.x, d.topk_idx, d.topk_w, d.w_gate_up, d.w_down, recompute=True)
+    torch.cuda.synchronize()
+    run.check()
+    assert_close("y", y.float().cpu().numpy(),
+                 oracle.moe_forward(x, idx, w, wgu, wd, r.act, limit, r.alpha))
+    ref = oracle.moe_backward(dy, x, idx, w, wgu, wd, r.act, limit, r.alpha)
+    assert_close("dx", grads[0].float().cpu().numpy(), ref[0])
+    assert_dw_close(grads[1].cpu().numpy(), ref[1])
+    assert_close("dw_gate_up", grads[2].cpu().numpy(), ref[2])
+    assert_close("dw_down", grads[3].cpu().numpy(), ref[3])
+    for name, a, b in zip(("dx", "d_topk_w", "dw_gate_up", "dw_down"), grads, again):
+        assert torch.equal(a, b), name
