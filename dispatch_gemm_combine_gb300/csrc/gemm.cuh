@@ -1037,9 +1037,11 @@ __global__ void __launch_bounds__(192, 1)
             }
           } else {  // kDgradDown
             // saved pre-activations of this row, gate at [0, I), up at [I, 2I):
-            // fp32, or fp16 (h1_half, see h1_code_gate).  Each lane copies its own row's 32 gate + 32 up
-            // values of a column chunk into shared memory with cp.async, one
-            // chunk ahead.
+            // fp32, or fp16 (h1_half, see h1_code_gate).  Each lane copies its
+            // own row's 32 gate + 32 up values of a column chunk into shared
+            // memory with cp.async, one chunk ahead.  A padding row reads
+            // nothing: its staging is zero-filled (its dA' and routing weight
+            // are zero, so its dH1 and w*a are zero whatever was saved).
             const int64_t h1off = static_cast<int64_t>(row) * 2 * args.I;   // elements
             const float* h1s = reinterpret_cast<const float*>(my_h1) + lane * 68;
             const uint32_t h1s_s = smem_u32(my_h1) + lane * 68 * 4;
@@ -1058,7 +1060,7 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
                   const int col = i0 + 8 * j;
-                  const bool in = col < args.I;
+                  const bool in = live && col < args.I;
                   cp_async16(h1s_s + j * 16, in ? h1row + col : h1row, in ? 16u : 0u);
                   cp_async16(h1s_s + 64 + j * 16, in ? h1row + args.I + col : h1row, in ? 16u : 0u);
                 }
@@ -1067,7 +1069,7 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
                   const int col = i0 + 4 * j;
-                  const bool in = col < args.I;
+                  const bool in = live && col < args.I;
                   cp_async16(h1s_s + j * 16, in ? h1row + col : h1row, in ? 16u : 0u);
                   cp_async16(h1s_s + 128 + j * 16, in ? h1row + args.I + col : h1row, in ? 16u : 0u);
                 }

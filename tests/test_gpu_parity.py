@@ -306,12 +306,6 @@ def test_expert_counts_at_tile_boundaries(k):
             assert torch.all(dwgu[e] == 0) and torch.all(dwd[e] == 0)
 
 
-def _bf16_ulp(v):
-    """Spacing of the bf16 values at |v| (2^(e-7) for |v| in [2^e, 2^(e+1)))."""
-    a = np.maximum(np.abs(v), np.finfo(np.float32).tiny)
-    return np.exp2(np.floor(np.log2(a)) - 7)
-
-
 @pytest.mark.parametrize("k", [1, 2])
 def test_expert_counts_at_tile_boundaries_heavy_tailed(k):
     """The tile-boundary counts with std-0.3 weights, where |y| and |dx| reach
@@ -327,7 +321,7 @@ def test_expert_counts_at_tile_boundaries_heavy_tailed(k):
     (d(topk w), every expert's weight gradients) keep the usual bounds."""
     from dispatch_gemm_combine_gb300 import MOE_BF16
     from dispatch_gemm_combine_gb300.runner import LayerRunner
-    from tests.helpers import MAX_ABS_RMS, REL_FROB, rel_frob
+    from tests.helpers import assert_close_bf16_output
     counts = [1, 15, 16, 17, 255, 256, 257, 271, 272, 273, 511, 512, 513, 0, 64, 65]
     E, H, I = len(counts), 128, 96
     slots = np.repeat(np.arange(E), counts)
@@ -348,13 +342,9 @@ def test_expert_counts_at_tile_boundaries_heavy_tailed(k):
     torch.cuda.synchronize()
     run.check()
     ref = oracle.moe_backward(dy, x, idx_np, w, wgu, wd, r.act)
-    for name, got, want in (("y", y, oracle.moe_forward(x, idx_np, w, wgu, wd, r.act)),
-                            ("dx", dx, ref[0])):
-        got = got.double().cpu().numpy()
-        rms = float(np.sqrt(np.mean(want ** 2)))
-        assert rel_frob(got, want) <= REL_FROB, name
-        excess = np.abs(got - want) - (MAX_ABS_RMS * rms + _bf16_ulp(want))
-        assert np.all(excess <= 0), (name, float(excess.max()) / rms)
+    assert_close_bf16_output("y", y.double().cpu().numpy(),
+                             oracle.moe_forward(x, idx_np, w, wgu, wd, r.act))
+    assert_close_bf16_output("dx", dx.double().cpu().numpy(), ref[0])
     assert_dw_close(dtw.cpu().numpy(), ref[1])
     for e in range(E):
         if counts[e]:
@@ -394,3 +384,46 @@ def test_clamped_glu_limits_and_saved_context(limit):
     assert_close("dw_down", grads[3].cpu().numpy(), ref[3])
     for name, a, b in zip(("dx", "d_topk_w", "dw_gate_up", "dw_down"), grads, again):
         assert torch.equal(a, b), name
+
+
+@pytest.mark.parametrize("act", [ACT_SWIGLU, ACT_CLAMPED_GLU])
+def test_weight_gradients_long_and_short_contractions(act):
+    """Two experts with 1100 and 1500 rows (contractions of 18 and 24 k-blocks,
+    one bf16 operand after the split selection) among 98 with 0-30 rows (hi +
+    lo operands, or zeros), several tiles per expert: every expert's weight
+    gradients against the oracle, and the layer's other outputs."""
+    from dispatch_gemm_combine_gb300 import MOE_BF16
+    from dispatch_gemm_combine_gb300.runner import LayerRunner
+    g = np.random.default_rng(71)
+    E, H, I = 100, 512, 256
+    counts = np.concatenate([[1100, 1500], g.integers(0, 31, E - 2)])
+    slots = np.repeat(np.arange(E), counts)
+    slots = slots[g.permutation(slots.size)]
+    T = slots.size
+    idx = torch.from_numpy(slots.reshape(T, 1).astype(np.int32))
+    r = _recipe(T, H, I, E, 1, act, seed=72, routing="uniform_ids", std=None)
+    case = synth.make_case(r)
+    case.topk_idx = idx
+    x, idx_np, w, wgu, wd, dy = oracle_inputs(case)
+    d = to_device(case)
+    run = LayerRunner(T, H, I, E, 1, act, MOE_BF16, r.limit, r.alpha)
+    run.plan(d.topk_idx)
+    y = run.forward(d.x, d.topk_idx, d.topk_w, d.w_gate_up, d.w_down).clone()
+    dx, dtw, dwgu, dwd = [t.clone() for t in run.backward(d.dy, d.x, d.topk_idx, d.topk_w,
+                                                          d.w_gate_up, d.w_down)]
+    torch.cuda.synchronize()
+    run.check()
+    # y and dx reach 11x their rms here (k = 1, weights U(0,1)): bf16 outputs
+    # are held to the bound with one bf16 step of headroom
+    from tests.helpers import assert_close_bf16_output
+    assert_close_bf16_output("y", y.double().cpu().numpy(),
+                             oracle.moe_forward(x, idx_np, w, wgu, wd, act))
+    ref = oracle.moe_backward(dy, x, idx_np, w, wgu, wd, act)
+    assert_close_bf16_output("dx", dx.double().cpu().numpy(), ref[0])
+    assert_dw_close(dtw.cpu().numpy(), ref[1])
+    for e in range(E):
+        if counts[e]:
+            assert_close("dw_gate_up[%d]" % e, dwgu[e].cpu().numpy(), ref[2][e])
+            assert_close("dw_down[%d]" % e, dwd[e].cpu().numpy(), ref[3][e])
+        else:
+            assert torch.all(dwgu[e] == 0) and torch.all(dwd[e] == 0)
