@@ -297,12 +297,15 @@ __device__ __forceinline__ uint32_t pack2<__half>(float a, float b) {
 }
 
 // Store this warp's 32x32 output tile: lane i holds row r0+i, columns
-// [c0, c0+32).  The tile goes through a per-warp shared-memory transpose
-// (rows padded so that both the row-wise writes and the column-wise reads
-// are free of bank conflicts), then every store instruction writes whole
-// rows: 8 lanes x 16 B = one 128-byte fp32 row segment, or 4 lanes x 16 B =
-// one 64-byte bf16 row segment.  Rows >= o.rows and columns >= o.cols are
-// not written.
+// [c0, c0+32).  The tile goes through a per-warp shared-memory transpose,
+// then every store instruction writes whole rows: 8 lanes x 16 B = one
+// 128-byte fp32 row segment, or 4 lanes x 16 B = one 64-byte 16-bit row
+// segment.  Both the row-wise writes and the segment-wise reads are free of
+// bank conflicts: fp32 rows are padded to 36 words; 16-bit rows are 64 bytes
+// (four 16-byte chunks) with chunk j of row i at position j ^ ((i >> 1) & 3),
+// so any 8 rows' chunk j (a write wavefront) and any 2 rows' 4 chunks (a read
+// wavefront) fall in 8 different 16-byte bank groups.  Rows >= o.rows and
+// columns >= o.cols are not written.
 template <typename O>
 __device__ __forceinline__ void store_tile(const OutDesc& o, int b, int r0, int c0,
                                            const float (&v)[32], uint8_t* stage, int lane) {
@@ -326,21 +329,21 @@ __device__ __forceinline__ void store_tile(const OutDesc& o, int b, int r0, int 
     }
     __syncwarp();
   } else {
-    __nv_bfloat16* st = reinterpret_cast<__nv_bfloat16*>(stage);
-    __nv_bfloat16* row = st + lane * 40;
+    uint4* st = reinterpret_cast<uint4*>(stage);   // [32 rows][4 chunks of 16 B]
+    const int sw = (lane >> 1) & 3;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const uint4 pk = make_uint4(pack2<O>(v[8 * j], v[8 * j + 1]), pack2<O>(v[8 * j + 2], v[8 * j + 3]),
                                   pack2<O>(v[8 * j + 4], v[8 * j + 5]),
                                   pack2<O>(v[8 * j + 6], v[8 * j + 7]));
-      *reinterpret_cast<uint4*>(row + 8 * j) = pk;
+      st[lane * 4 + (j ^ sw)] = pk;
     }
     __syncwarp();
     const int c = (lane & 3) * 8;
 #pragma unroll
     for (int it = 0; it < 4; ++it) {
       const int r = it * 8 + (lane >> 2);
-      const uint4 val = *reinterpret_cast<const uint4*>(st + r * 40 + c);
+      const uint4 val = st[r * 4 + ((lane & 3) ^ ((r >> 1) & 3))];
       const int gr = r0 + r, gc = c0 + c;
       if (gr < o.rows && gc < o.cols)
         *reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(base) +
