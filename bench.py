@@ -600,6 +600,30 @@ def main():
     # the results that came back are the layer's (same inputs every step)
     assert torch.equal(h_out[(n_e2e - 1) % 2]["dx"], run.dx.cpu())
 
+    # ---- the expert-parallel path on this one rank (§8(f) row 4): its
+    # exchanges are identities here, so this times its own steps (two row
+    # gathers, the owner-side layer at k = 1, the fp32 combine and the host
+    # round trip of the counts each forward makes) against the fused layer,
+    # and checks that it returns the same y and dx bit for bit
+    from dispatch_gemm_combine_gb300.expert_parallel import CudaOps, ExpertParallelMoE
+    run.plan(case.topk_idx)
+    y_ref = run.forward(case.x, case.topk_idx, case.topk_w, case.w_gate_up, case.w_down).clone()
+    dx_ref = run.backward(case.dy, case.x, case.topk_idx, case.topk_w, case.w_gate_up,
+                          case.w_down)[0].clone()
+    ep = ExpertParallelMoE(r.E, r.k, CudaOps(r.H, r.I, r.act, dt, r.limit, r.alpha))
+
+    def ep_step():
+        ep.forward(case.x, case.topk_idx, case.topk_w, case.w_gate_up, case.w_down)
+        return ep.backward(case.dy)
+
+    ep_step()
+    ep_y = ep.forward(case.x, case.topk_idx, case.topk_w, case.w_gate_up, case.w_down)
+    ep_dx = ep.backward(case.dy)[0]
+    ep_same = bool(torch.equal(ep_y, y_ref) and torch.equal(ep_dx, dx_ref))
+    ep_calls = timed_calls(ep_step, max(3, min(args.steps, 10)), stream)
+    del ep, ep_y, ep_dx, y_ref, dx_ref
+    torch.cuda.empty_cache()
+
     # ---- accounting
     e_active = int((run.plan_t["counts"] > 0).sum().item())
 
@@ -697,6 +721,13 @@ def main():
         "gpu_launches": int(launches),
         "router": {"ms": round(route_ms, 4), "what": "moe_route: fp32 logits [T,E] -> top-%d ids, "
                    "softmax weights and the dispatch plan (outside the layer metric)" % r.k},
+        "expert_parallel": {"ranks": 1, "ms": stats_ms(ep_calls),
+                            "overhead_vs_layer": round(statistics.median(ep_calls) /
+                                                       (fwd_ms + bwd_ms) - 1.0, 4),
+                            "bitwise_equal_to_layer": ep_same,
+                            "what": "ExpertParallelMoE fwd+bwd on one rank (exchanges are "
+                                    "identities): plan, row gathers, the owner-side layer at "
+                                    "k = 1, fp32 combine, one host read of the counts"},
         "clocks": clocks.summary(),
         "experts_active": e_active,
     }

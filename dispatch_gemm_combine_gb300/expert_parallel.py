@@ -99,7 +99,9 @@ class ExpertParallelMoE:
     def _bounds(self):
         return [expert_range(self.E, self.world, q) for q in range(self.world)]
 
-    def forward(self, x, topk_idx, topk_w, w_gate_up, w_down):
+    def forward(self, x, topk_idx, topk_w, w_gate_up, w_down, b_gate_up=None, b_down=None):
+        """y [T,H] for this rank's tokens.  b_gate_up [E_loc,2I] / b_down
+        [E_loc,H]: the optional per-expert biases of this rank's experts."""
         ops, k = self.ops, self.k
         T = topk_idx.shape[0]
         Tk = T * k
@@ -121,13 +123,16 @@ class ExpertParallelMoE:
         ids = np.repeat(np.tile(np.arange(self.E_loc, dtype=np.int32), self.world),
                         recv_counts.reshape(-1))
         ids = ops.to_device(torch.from_numpy(ids.reshape(-1, 1)))
-        yr, ctx = ops.expert_forward(xr, ids, wr, self.E_loc, w_gate_up, w_down)
+        yr, ctx = ops.expert_forward(xr, ids, wr, self.E_loc, w_gate_up, w_down, b_gate_up,
+                                     b_down)
         ys = self.x.rows(yr, recv, send)
         y = ops.combine(p["inv"], ys, T, k, like=x)
         self._ctx = (p, send, recv, ctx, T)
         return y
 
     def backward(self, dy):
+        """(dx, d_topk_w, dw_gate_up, dw_down) and, with biases, (db_gate_up,
+        db_down) of this rank's experts."""
         if self._ctx is None:
             raise RuntimeError("backward() needs a forward() first")
         ops, k = self.ops, self.k
@@ -135,22 +140,26 @@ class ExpertParallelMoE:
         Tk = T * k
         dys = ops.gather(p["perm"], k, dy, Tk)
         dyr = self.x.rows(dys, send, recv)
-        dxr, dwr, dwgu, dwd = ops.expert_backward(ctx, dyr)
+        g = ops.expert_backward(ctx, dyr)
+        dxr, dwr = g[0], g[1]
         dxs = self.x.rows(dxr, recv, send)
         dws = self.x.rows(dwr.reshape(-1, 1), recv, send)
         dx = ops.combine(p["inv"], dxs, T, k, like=dy)
         d_topk_w = ops.gather(p["inv"], 1, dws, Tk).reshape(T, k)
         self._ctx = None
-        return dx, d_topk_w, dwgu, dwd
+        return (dx, d_topk_w) + tuple(g[2:])
 
 
 class CudaOps:
     """The steps of the expert-parallel layer on the GPU, through the C ABI.
     Tensors live on `device`; the collectives run on the same device (NCCL)."""
 
-    def __init__(self, H, I, act, dtype=MOE_BF16, clamp_limit=7.0, alpha=1.702, device="cuda"):
+    def __init__(self, H, I, act, dtype=MOE_BF16, clamp_limit=7.0, alpha=1.702, device="cuda",
+                 gate_up_layout=0):
         self.H, self.I, self.act, self.dtype = H, I, act, dtype
         self.limit, self.alpha, self.device = clamp_limit, alpha, device
+        self.layout = gate_up_layout
+        self._run = None   # the owner-side buffers, kept while the row count repeats
 
     def to_comm(self, t):
         return t.to(self.device)
@@ -186,19 +195,26 @@ class CudaOps:
             combine_rows(shape, inv, src.contiguous(), dst)
         return dst
 
-    def expert_forward(self, x_rows, ids, w_rows, E_loc, w_gate_up, w_down):
+    def expert_forward(self, x_rows, ids, w_rows, E_loc, w_gate_up, w_down, b_gate_up=None,
+                       b_down=None):
         n = x_rows.shape[0]
-        run = LayerRunner(n, self.H, self.I, max(E_loc, 1), 1, self.act, self.dtype, self.limit,
-                          self.alpha, device=self.device, out_fp32=True)
-        ctx = (run, x_rows, ids, w_rows.reshape(-1, 1).contiguous(), w_gate_up, w_down)
+        key = (n, max(E_loc, 1))
+        if self._run is None or self._run[0] != key:
+            self._run = (key, LayerRunner(n, self.H, self.I, key[1], 1, self.act, self.dtype,
+                                          self.limit, self.alpha, device=self.device,
+                                          gate_up_layout=self.layout, out_fp32=True))
+        run = self._run[1]
+        ctx = (run, x_rows, ids, w_rows.reshape(-1, 1).contiguous(), w_gate_up, w_down, b_gate_up,
+               b_down)
         if n:
             run.plan(ids)
-            run.forward(x_rows, ids, ctx[3], w_gate_up, w_down)
+            run.forward(x_rows, ids, ctx[3], w_gate_up, w_down, b_gate_up=b_gate_up,
+                        b_down=b_down)
         return run.y, ctx
 
     def expert_backward(self, ctx, dy_rows):
-        run, x_rows, ids, w_rows, w_gate_up, w_down = ctx
-        dx, dw, dwgu, dwd = run.backward(dy_rows.contiguous(), x_rows, ids, w_rows, w_gate_up,
-                                         w_down)
+        run, x_rows, ids, w_rows, w_gate_up, w_down, b_gate_up, b_down = ctx
+        g = run.backward(dy_rows.contiguous(), x_rows, ids, w_rows, w_gate_up, w_down,
+                         b_gate_up=b_gate_up, b_down=b_down)
         run.check()
-        return dx, dw.reshape(-1), dwgu, dwd
+        return (g[0], g[1].reshape(-1)) + tuple(g[2:])

@@ -49,7 +49,8 @@ class OracleOps:
     def combine(self, inv, src, T, k, like):
         return src[inv.long()].reshape(T, k, -1).sum(dim=1)
 
-    def expert_forward(self, x_rows, ids, w_rows, E_loc, w_gate_up, w_down):
+    def expert_forward(self, x_rows, ids, w_rows, E_loc, w_gate_up, w_down, b_gate_up=None,
+                       b_down=None):
         w = w_rows.reshape(-1, 1).numpy()
         y = oracle.moe_forward(x_rows.numpy(), ids.numpy(), w, w_gate_up, w_down, self.act)
         return torch.from_numpy(np.ascontiguousarray(y)), (x_rows.numpy(), ids.numpy(), w,

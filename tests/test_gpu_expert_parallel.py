@@ -77,3 +77,35 @@ def test_expert_parallel_single_rank(act, E):
     assert_dw_close(dtw.cpu().numpy(), ref[1])
     assert_close("dw_gate_up", dwgu.cpu().numpy(), ref[2])
     assert_close("dw_down", dwd.cpu().numpy(), ref[3])
+
+
+def test_expert_parallel_single_rank_is_the_layer_bit_for_bit():
+    """On one rank every exchange is an identity and the owner's plan sees the
+    rows in the layer's own expert-grouped order, so the owner runs the same
+    tiles on the same rows; with fp32 owner outputs and the same fixed-order
+    combine, y, dx, d(topk w), the weight gradients and the bias gradients
+    equal the fused layer's bit for bit."""
+    from dispatch_gemm_combine_gb300 import MOE_BF16
+    from dispatch_gemm_combine_gb300.expert_parallel import CudaOps, ExpertParallelMoE
+    from dispatch_gemm_combine_gb300.runner import LayerRunner
+    r = Recipe("ep", T=1024, H=512, I=384, E=16, k=4, act=ACT_CLAMPED_GLU, weight_std=0.05,
+               routing="uniform_topk_softmax", seed=31)
+    case = synth.make_case(r)
+    d = to_device(case)
+    bgu, bd = (t.cuda() for t in synth.make_biases(r))
+    run = LayerRunner(r.T, r.H, r.I, r.E, r.k, r.act, MOE_BF16, r.limit, r.alpha)
+    run.plan(d.topk_idx)
+    y = run.forward(d.x, d.topk_idx, d.topk_w, d.w_gate_up, d.w_down, b_gate_up=bgu,
+                    b_down=bd).clone()
+    ref = [t.clone() for t in run.backward(d.dy, d.x, d.topk_idx, d.topk_w, d.w_gate_up,
+                                           d.w_down, b_gate_up=bgu, b_down=bd)]
+    ep = ExpertParallelMoE(r.E, r.k, CudaOps(r.H, r.I, r.act, MOE_BF16, r.limit, r.alpha))
+    for _ in range(2):   # twice: the owner's buffers are reused
+        y2 = ep.forward(d.x, d.topk_idx, d.topk_w, d.w_gate_up, d.w_down, bgu, bd)
+        got = ep.backward(d.dy)
+        torch.cuda.synchronize()
+        run.check()
+        assert torch.equal(y2, y)
+        for name, a, b in zip(("dx", "d_topk_w", "dw_gate_up", "dw_down", "db_gate_up",
+                               "db_down"), got, ref):
+            assert torch.equal(a, b), name
