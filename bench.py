@@ -27,6 +27,8 @@ import sys
 import threading
 import time
 
+import numpy as np
+
 ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
@@ -58,23 +60,29 @@ def layer_bytes(r, e_active):
 
 
 def kernel_work(r, e_active):
-    """Per-launch algorithmic FLOPs and compulsory bytes of each kernel kind
-    (its operands and outputs at their stored precision, useful rows only)."""
+    """Per-launch algorithmic FLOPs and compulsory bytes of each kernel kind:
+    its operands and outputs once each, at their stored precision, useful rows
+    only.  The saved pre-activations count at their stored width (fp16 for the
+    clamped GLU with bf16 storage and an fp16 clamp limit, else fp32); the
+    weight gradients' computed operands (dH1, w*a) count once, without the
+    bf16 remainder some experts carry for precision."""
     es = 2 if r.dtype == "bf16" else 4
     T, H, I, E, k = r.T, r.H, r.I, r.E, r.k
     Tk = T * k
+    h1 = 2 if (es == 2 and r.act == 1 and float(np.float16(r.limit)) == r.limit
+               and abs(r.limit) <= 32768) else 4
     wgu = e_active * H * 2.0 * I * es
     wd = e_active * I * H * es
     return {
         "gather_rows": (0.0, T * H * es + Tk * H * es),
-        "gemm_fwd_gate_up_act": (4.0 * Tk * H * I, Tk * H * es + wgu + Tk * I * es + Tk * 2 * I * 4),
+        "gemm_fwd_gate_up_act": (4.0 * Tk * H * I, Tk * H * es + wgu + Tk * I * es + Tk * 2 * I * h1),
         "gemm_fwd_down_scale": (2.0 * Tk * I * H, Tk * I * es + wd + Tk * H * 4),
         "combine": (0.0, Tk * H * 4.0 + T * H * es),
         "gemm_dgrad_down_act_bwd": (2.0 * Tk * H * I,
-                                    Tk * H * es + wd + Tk * 2 * I * 4 + Tk * 3 * I * es * 2),
-        "gemm_wgrad_down": (2.0 * Tk * I * H, Tk * I * es * 2 + Tk * H * es + E * I * H * 4.0),
+                                    Tk * H * es + wd + Tk * 2 * I * h1 + Tk * 3 * I * es),
+        "gemm_wgrad_down": (2.0 * Tk * I * H, Tk * I * es + Tk * H * es + E * I * H * 4.0),
         "gemm_dgrad_gate_up": (4.0 * Tk * I * H, Tk * 2 * I * es + wgu + Tk * H * 4),
-        "gemm_wgrad_gate_up": (4.0 * Tk * H * I, Tk * H * es + Tk * 2 * I * es * 2 + E * H * 2.0 * I * 4),
+        "gemm_wgrad_gate_up": (4.0 * Tk * H * I, Tk * H * es + Tk * 2 * I * es + E * H * 2.0 * I * 4),
     }
 
 
