@@ -83,17 +83,22 @@ struct GemmCfg {
   // the workspace first); 16-bit operands may be MN-major.
   static constexpr bool A_MN = (kWgrad || (SW && MODE == kFwdDown)) && !kTf32;
   static constexpr bool B_MN = !SW && (MODE == kFwdGateUp || MODE == kFwdDown || kWgrad) && !kTf32;
-  // bf16 weight gradients contract a computed operand (w*a, dH1) that is
-  // carried as a bf16 hi/lo pair: two MMAs, one per part, into the same
-  // accumulator (about 16 bits of mantissa instead of 8).
+  // bf16 weight gradients contract a computed operand (w*a, dH1) that the
+  // experts with few effectively weighted rows carry as a bf16 hi/lo pair:
+  // two MMAs, one per part, into the same accumulator (about 16 bits of
+  // mantissa instead of 8).  A k-block of such an expert takes two slots of
+  // the shared-memory ring: the operands (hi part) in one, the lo part in
+  // the next, each slot with its own barriers; every other k-block takes
+  // one, so the ring is as deep as the slots allow.
   static constexpr bool SPLIT_A = (MODE == kWgradDown) && !kTf32;
   static constexpr bool SPLIT_B = (MODE == kWgradGateUp) && !kTf32;
   static constexpr int BN_CTA = BN / PAIR;       // B columns held by one CTA
   static constexpr int A_PART = 128 * 128;       // 128 rows of A, one 128-byte K row each
   static constexpr int B_PART = BN_CTA * 128;
-  static constexpr int A_BYTES = A_PART * (SPLIT_A ? 2 : 1);
-  static constexpr int B_BYTES = B_PART * (SPLIT_B ? 2 : 1);
-  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;   // per CTA
+  static constexpr int A_BYTES = A_PART;
+  static constexpr int B_BYTES = B_PART;
+  static constexpr int LO_BYTES = SPLIT_A ? A_PART : (SPLIT_B ? B_PART : 0);
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;   // per CTA and ring slot
   static constexpr int CHUNK_BYTES = BK * 128;   // one MN-major box
   // per epilogue warp: one 32x32 transpose tile, rows padded to 36 words;
   // the down dgrad also stages the saved pre-activations of its 32 rows
@@ -558,6 +563,13 @@ __global__ void __launch_bounds__(192, 1)
   const int unit0 = blockIdx.x / C::PAIR;
   const int ustride = gridDim.x / C::PAIR;
   const uint64_t tmo = args.timeout_ns;
+  // next slot of the shared-memory ring; the barrier parity flips per lap
+  auto ring_next = [](int& s, uint32_t& p) {
+    if (++s == STAGES) {
+      s = 0;
+      p ^= 1u;
+    }
+  };
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -567,9 +579,17 @@ __global__ void __launch_bounds__(192, 1)
     bool ok = true;
     for (int t = unit0; t < total && ok; t += ustride) {
       const TileInfo ti = decode_tile<C::BN_OUT, C::kWgrad, C::PAIR, C::SW>(args, t, C::BK, crank);
+      // a split operand's expert: the lo part of each k-block in the next slot
+      const bool two = C::LO_BYTES > 0 && ti.lo;
       for (int kb = 0; kb < ti.nkb; ++kb) {
+        int stage2 = stage;
+        uint32_t phase2 = phase;
+        if (two) ring_next(stage2, phase2);
         int good = 1;
-        if (lane == 0) good = mbar_wait(empty_bar + 8 * stage, phase ^ 1u, tmo);
+        if (lane == 0) {
+          good = mbar_wait(empty_bar + 8 * stage, phase ^ 1u, tmo);
+          if (good && two) good = mbar_wait(empty_bar + 8 * stage2, phase2 ^ 1u, tmo);
+        }
         good = __shfl_sync(0xffffffffu, good, 0);
         if (!good) {
           if (lane == 0) record_error(args.err, kErrTimeout);
@@ -581,20 +601,26 @@ __global__ void __launch_bounds__(192, 1)
           const uint32_t fbt = leader_addr(fb);
           const uint32_t sA = s_stages + stage * C::STAGE_BYTES;
           const uint32_t sB = sA + C::A_BYTES;
+          // the lo part's slot (two-slot k-blocks)
+          const uint32_t fb2 = full_bar + 8 * stage2;
+          const uint32_t fbt2 = leader_addr(fb2);
+          const uint32_t sA2 = s_stages + stage2 * C::STAGE_BYTES;
+          const uint32_t sB2 = sA2 + C::A_BYTES;
           // token-N tiling: a unit of at most 64 tokens (32 rows per CTA)
           // loads its token rows with the 32-row box of maps.a2
           const bool small_b = C::SW && ti.nn <= 64;
-          // a split operand's lo part is loaded only for experts that need it
-          constexpr uint32_t kLoBytes = C::SPLIT_A ? C::A_PART : (C::SPLIT_B ? C::B_PART : 0);
-          const uint32_t stage_tx = small_b ? C::A_BYTES + 32 * 128
-                                            : C::STAGE_BYTES - (ti.lo ? 0u : kLoBytes);
+          const uint32_t stage_tx = small_b ? C::A_BYTES + 32 * 128 : C::STAGE_BYTES;
           // the leader expects the bytes of both CTAs of the pair
-          if (leader) mbar_arrive_expect_tx(fb, C::PAIR * stage_tx);
-          auto load2 = [&](uint32_t dst, const CUtensorMap* m, int c0, int c1) {
+          if (leader) {
+            mbar_arrive_expect_tx(fb, C::PAIR * stage_tx);
+            if (two) mbar_arrive_expect_tx(fb2, C::PAIR * C::LO_BYTES);
+          }
+          auto load2 = [&](uint32_t dst, const CUtensorMap* m, int c0, int c1, uint32_t bar = 0) {
+            if (bar == 0) bar = fbt;
             if constexpr (C::CTA2)
-              tma_load_2d_g2(dst, m, fbt, c0, c1);
+              tma_load_2d_g2(dst, m, bar, c0, c1);
             else
-              tma_load_2d(dst, m, fbt, c0, c1);
+              tma_load_2d(dst, m, bar, c0, c1);
           };
           auto load3 = [&](uint32_t dst, const CUtensorMap* m, int c0, int c1, int c2) {
             if constexpr (C::CTA2)
@@ -622,14 +648,15 @@ __global__ void __launch_bounds__(192, 1)
           } else if constexpr (!C::A_MN) {
             load2(sA, &maps.a, kc, ti.row0);
           } else {
-            // MN-major chunks (128 B of M x BK rows): hi, then lo when split
+            // MN-major chunks (128 B of M x BK rows); a split A's lo part in
+            // the next slot
 #pragma unroll
-            for (int part = 0; part < (C::SPLIT_A ? 2 : 1); ++part) {
-              if (part && !ti.lo) break;
+            for (int c = 0; c < 128 / C::CH; ++c)
+              load2(sA + c * C::CHUNK_BYTES, &maps.a, ti.m0 + c * C::CH, ti.row0 + kc);
+            if (C::SPLIT_A && two) {
 #pragma unroll
               for (int c = 0; c < 128 / C::CH; ++c)
-                load2(sA + part * C::A_PART + c * C::CHUNK_BYTES, part ? &maps.a2 : &maps.a,
-                      ti.m0 + c * C::CH, ti.row0 + kc);
+                load2(sA2 + c * C::CHUNK_BYTES, &maps.a2, ti.m0 + c * C::CH, ti.row0 + kc, fbt2);
             }
           }
           // ---- B: this CTA's BN_CTA columns
@@ -665,22 +692,21 @@ __global__ void __launch_bounds__(192, 1)
             load2(sB, &maps.b0, ti.row0 + kc, nb);
           } else {
 #pragma unroll
-            for (int part = 0; part < (C::SPLIT_B ? 2 : 1); ++part) {
-              if (part && !ti.lo) break;
+            for (int c = 0; c < C::BN_CTA / C::CH; ++c)
+              load2(sB + c * C::CHUNK_BYTES, &maps.b0, nb + c * C::CH, ti.row0 + kc);
+            if (C::SPLIT_B && two) {   // a split B's lo part in the next slot
 #pragma unroll
               for (int c = 0; c < C::BN_CTA / C::CH; ++c)
-                load2(sB + part * C::B_PART + c * C::CHUNK_BYTES, part ? &maps.b1 : &maps.b0,
-                      nb + c * C::CH, ti.row0 + kc);
+                load2(sB2 + c * C::CHUNK_BYTES, &maps.b1, nb + c * C::CH, ti.row0 + kc, fbt2);
             }
           }
           }
         }
         __syncwarp();
-        ++issued;
-        if (++stage == STAGES) {
-          stage = 0;
-          phase ^= 1u;
-        }
+        // (each slot used counts once: the drain below waits for every use)
+        issued += two ? 2 : 1;
+        ring_next(stage, phase);
+        if (two) ring_next(stage, phase);
       }
     }
     // Before the CTAs may exit, every load issued must have landed: the
@@ -713,8 +739,15 @@ __global__ void __launch_bounds__(192, 1)
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * C::ACC_COLS;
+        const bool two = C::LO_BYTES > 0 && ti.lo;   // (as in the producer)
         for (int kb = 0; kb < ti.nkb; ++kb) {
-          if (lane == 0) good = mbar_wait(full_bar + 8 * stage, phase, tmo);
+          int stage2 = stage;
+          uint32_t phase2 = phase;
+          if (two) ring_next(stage2, phase2);
+          if (lane == 0) {
+            good = mbar_wait(full_bar + 8 * stage, phase, tmo);
+            if (good && two) good = mbar_wait(full_bar + 8 * stage2, phase2, tmo);
+          }
           good = __shfl_sync(0xffffffffu, good, 0);
           if (!good) {
             if (lane == 0) record_error(args.err, kErrTimeout);
@@ -725,6 +758,8 @@ __global__ void __launch_bounds__(192, 1)
           if (lane == 0) {
             const uint32_t sA = s_stages + stage * C::STAGE_BYTES;
             const uint32_t sB = sA + C::A_BYTES;
+            const uint32_t sA2 = s_stages + stage2 * C::STAGE_BYTES;   // lo part (two slots)
+            const uint32_t sB2 = sA2 + C::A_BYTES;
             const uint32_t idesc =
                 C::SW ? make_idesc(C::kTf32, C::A_MN, C::B_MN, 256, ti.nn)
                       : (ti.half ? C::IDESC_HALF : C::IDESC);
@@ -748,21 +783,22 @@ __global__ void __launch_bounds__(192, 1)
               const uint64_t bdesc = smem_desc_sw128(sB + boff, blbo, 1024);
               mma(adesc, bdesc, (kb | kk) != 0 ? 1u : 0u);
               if constexpr (C::SPLIT_A)
-                if (ti.lo) mma(smem_desc_sw128(sA + C::A_PART + aoff, albo, 1024), bdesc, 1u);
+                if (two) mma(smem_desc_sw128(sA2 + aoff, albo, 1024), bdesc, 1u);
               if constexpr (C::SPLIT_B)
-                if (ti.lo) mma(adesc, smem_desc_sw128(sB + C::B_PART + boff, blbo, 1024), 1u);
+                if (two) mma(adesc, smem_desc_sw128(sB2 + boff, blbo, 1024), 1u);
             }
-            // the stage is free in both CTAs once these MMAs have read it
-            if constexpr (C::CTA2)
+            // the slots are free in both CTAs once these MMAs have read them
+            if constexpr (C::CTA2) {
               tc_commit2_mc(empty_bar + 8 * stage, kPairMask);
-            else
+              if (two) tc_commit2_mc(empty_bar + 8 * stage2, kPairMask);
+            } else {
               tc_commit(empty_bar + 8 * stage);
+              if (two) tc_commit(empty_bar + 8 * stage2);
+            }
           }
           __syncwarp();
-          if (++stage == STAGES) {
-            stage = 0;
-            phase ^= 1u;
-          }
+          ring_next(stage, phase);
+          if (two) ring_next(stage, phase);
         }
         if (!ok) break;
         if (lane == 0) {

@@ -8,8 +8,8 @@ cudaError_t launch_gemm_bf16_wgrad(int mode, const GemmMaps& maps, const GemmArg
                                    cudaStream_t st) {
   using T = __nv_bfloat16;
   switch (mode) {
-    case kWgradDown: return launch_gemm_t<T, kWgradDown, 256, 4>(maps, a, sms, st);
-    case kWgradGateUp: return launch_gemm_t<T, kWgradGateUp, 256, 4>(maps, a, sms, st);
+    case kWgradDown: return launch_gemm_t<T, kWgradDown, 256, 6>(maps, a, sms, st);
+    case kWgradGateUp: return launch_gemm_t<T, kWgradGateUp, 256, 6>(maps, a, sms, st);
     default: return cudaErrorInvalidValue;
   }
 }
