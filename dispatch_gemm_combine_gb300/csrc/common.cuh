@@ -358,25 +358,6 @@ __device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&v)[64]) {
   for (int i = 0; i < 64; ++i) v[i] = __uint_as_float(r[i]);
 }
 
-// 16 lanes x 64 columns (8 repetitions of 8): thread t of the warp receives
-// rows (t/4) and (t/4)+8 of the 16-lane block at columns 8j + 2(t%4) and
-// 8j + 2(t%4) + 1 of repetition j, as v[4j..4j+3] = (row a, c), (row a, c+1),
-// (row b, c), (row b, c+1).  Four consecutive lanes hold 32 contiguous bytes
-// of a row, so the values can be stored to global memory as full sectors
-// without a shared-memory transpose.  The wait is part of the statement.
-__device__ __forceinline__ void tmem_ld16x64(uint32_t taddr, float (&v)[32]) {
-  uint32_t r[32];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.16x256b.x8.b32 "
-      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];\n\t"
-      "tcgen05.wait::ld.sync.aligned;"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-      : "r"(taddr)
-      : "memory");
-#pragma unroll
-  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-}
-
 // Shared-memory matrix descriptor for tcgen05.mma with the 128-byte swizzle
 // (the layout TMA writes with CU_TENSOR_MAP_SWIZZLE_128B): start address,
 // leading-dimension byte offset, stride-dimension byte offset, the fixed

@@ -103,12 +103,12 @@ struct GemmCfg {
   // per epilogue warp: one 32x32 transpose tile, rows padded to 36 words;
   // the down dgrad also stages the saved pre-activations of its 32 rows
   // (32 gate + 32 up fp32 per row, rows padded to 68 words)
-  // The down weight gradient stores its fp32 tiles with TMA (measured 12%
-  // faster than register stores).  The gate_up one, which writes twice the
-  // bytes, measured 2% slower that way, and the fp32 rows of the forward
-  // down GEMM and the gate_up dgrad measured within 2% of the shared-memory
-  // transposes, so those keep the register paths.
-  static constexpr bool TMA_OUT = (MODE == kWgradDown);
+  // The weight gradients store their fp32 tiles with TMA tensor stores
+  // (measured 12% faster than register stores on the down one, 13% on the
+  // gate_up one); the fp32 rows of the forward down GEMM and the gate_up
+  // dgrad measured within 2% of the shared-memory transposes, so those keep
+  // the register paths.
+  static constexpr bool TMA_OUT = kWgrad;
   // (TMA_OUT: two 32 x 32 fp32 tiles in the 128-byte swizzle, the staging
   // of the tensor stores)
   static constexpr int EPI_WARP_BYTES = TMA_OUT ? 2 * 4096 : 32 * 36 * 4;
@@ -386,28 +386,6 @@ __device__ __forceinline__ void store_tile_t(const OutDesc& o, int r0, int c0,
       *reinterpret_cast<float4*>(base + static_cast<int64_t>(r0 + r) * o.ld + gc) = val;
   }
   __syncwarp();
-}
-
-// Store a 16-row x 64-column fp32 block read with tmem_ld16x64 straight from
-// registers: lane t writes 8 bytes at rows r0 + t/4 and r0 + 8 + t/4, so four
-// lanes fill one 32-byte sector.  Rows >= o.rows and columns >= o.cols (a
-// multiple of 8) are not written.
-__device__ __forceinline__ void store_rows16(const OutDesc& o, int b, int r0, int c0,
-                                             const float (&v)[32], int lane) {
-  float* base = static_cast<float*>(o.ptr) + static_cast<int64_t>(b) * o.bstride;
-  const int ra = r0 + (lane >> 2), rb = ra + 8;
-  const int cc = c0 + 2 * (lane & 3);
-  float* pa = base + static_cast<int64_t>(ra) * o.ld;
-  float* pb = base + static_cast<int64_t>(rb) * o.ld;
-#pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    const int col = cc + 8 * j;
-    if (col < o.cols) {
-      if (ra < o.rows) *reinterpret_cast<float2*>(pa + col) = make_float2(v[4 * j], v[4 * j + 1]);
-      if (rb < o.rows)
-        *reinterpret_cast<float2*>(pb + col) = make_float2(v[4 * j + 2], v[4 * j + 3]);
-    }
-  }
 }
 
 // Stage lane r's 32 fp32 values as row r of a 32 x 32 tile in the 128-byte
@@ -912,21 +890,6 @@ __global__ void __launch_bounds__(192, 1)
                          min(32, live - c * 32), [&](int r) {
                            return MODE == kFwdDown ? __shfl_sync(0xffffffffu, wc, r) : 1.f;
                          });
-          }
-        } else if constexpr (C::kWgrad && !C::TMA_OUT) {
-          // fp32 weight gradients go straight from tensor memory to global
-          // memory in 16-row x 64-column blocks
-#pragma unroll 1
-          for (int blk = 0; blk < (BN / 64) * 2; ++blk) {
-            const int c = blk / 2, hf = blk & 1;
-            float w2[32];
-            if (ti.nkb > 0) {
-              tmem_ld16x64(tacc + (static_cast<uint32_t>(hf * 16) << 16) + c * 64, w2);
-            } else {
-#pragma unroll
-              for (int i = 0; i < 32; ++i) w2[i] = 0.f;
-            }
-            store_rows16(args.out[0], ti.e, ti.m0 + q * 32 + hf * 16, ti.n0 + c * 64, w2, lane);
           }
         } else if constexpr (C::kWgrad) {
           // fp32 weight gradients leave through TMA tensor stores: per 32-column
