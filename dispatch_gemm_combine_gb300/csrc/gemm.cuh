@@ -109,12 +109,18 @@ struct GemmCfg {
   // dgrad measured within 2% of the shared-memory transposes, so those keep
   // the register paths.
   static constexpr bool TMA_OUT = kWgrad;
-  // (TMA_OUT: two 32 x 32 fp32 tiles in the 128-byte swizzle, the staging
-  // of the tensor stores)
-  static constexpr int EPI_WARP_BYTES = TMA_OUT ? 2 * 4096 : 32 * 36 * 4;
   static constexpr int H1_WARP_BYTES = (MODE == kDgradDown) ? 32 * 68 * 4 : 0;
-  static constexpr int EPI_BYTES = 4 * (EPI_WARP_BYTES + H1_WARP_BYTES);
   static constexpr int BAR_BYTES = (2 * STAGES + 5) * 8 + 16;
+  // TMA_OUT: each epilogue warp stages its stores in STG_BUFS 32 x 32 fp32
+  // tiles (128-byte swizzle), as many as the shared memory left beside the
+  // ring holds (2 to 6).  A tile may be rewritten only once the store that
+  // read it has left shared memory, so the staging bounds the store bytes a
+  // warp keeps in flight.
+  static constexpr int STG_AVAIL = 232448 - 1024 - STAGES * STAGE_BYTES - BAR_BYTES;
+  static constexpr int STG_BUFS =
+      STG_AVAIL / (4 * 4096) > 6 ? 6 : (STG_AVAIL / (4 * 4096) < 2 ? 2 : STG_AVAIL / (4 * 4096));
+  static constexpr int EPI_WARP_BYTES = TMA_OUT ? STG_BUFS * 4096 : 32 * 36 * 4;
+  static constexpr int EPI_BYTES = 4 * (EPI_WARP_BYTES + H1_WARP_BYTES);
   static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + EPI_BYTES + BAR_BYTES;
   static constexpr int ACC_COLS = BN;            // TMEM columns of one tile's accumulator
   static constexpr int TMEM_COLS = (2 * ACC_COLS <= 256) ? 256 : 512;
@@ -391,11 +397,13 @@ __device__ __forceinline__ void store_tile_t(const OutDesc& o, int r0, int c0,
 // Stage lane r's 32 fp32 values as row r of a 32 x 32 tile in the 128-byte
 // swizzle at `buf` (1024-byte aligned; conflict-free 16-byte stores) and
 // store the tile at (x, y, z) of `map` with one TMA tensor store issued by
-// lane 0.  Callers alternate two buffers: the wait keeps at most one earlier
-// store still reading shared memory, i.e. the other buffer's.
+// lane 0.  Callers cycle through NBUF buffers, one bulk group per use: the
+// wait leaves at most NBUF - 1 later groups reading shared memory, so the
+// last store from `buf` has read it.
+template <int NBUF>
 __device__ __forceinline__ void tma_store_tile32(const CUtensorMap* map, uint32_t buf,
                                                  const float* v, int x, int y, int z, int lane) {
-  if (lane == 0) bulk_wait_read<1>();
+  if (lane == 0) bulk_wait_read<NBUF - 1>();
   __syncwarp();
 #pragma unroll
   for (int j = 0; j < 8; ++j)
@@ -815,11 +823,11 @@ __global__ void __launch_bounds__(192, 1)
     uint8_t* my_h1 = my_epi + C::EPI_WARP_BYTES;
     int acc = 0;
     uint32_t acc_phase = 0;
-    // TMA_OUT staging: the next of this warp's two 32 x 32 fp32 tiles
+    // TMA_OUT staging: the next of this warp's STG_BUFS 32 x 32 fp32 tiles
     uint32_t stg_next = 0;
     auto stg_buf = [&]() -> uint32_t {
       const uint32_t b = smem_u32(my_epi) + stg_next * 4096;
-      stg_next ^= 1u;
+      stg_next = (stg_next + 1 == C::STG_BUFS) ? 0u : stg_next + 1;
       return b;
     };
 
@@ -895,18 +903,31 @@ __global__ void __launch_bounds__(192, 1)
           // fp32 weight gradients leave through TMA tensor stores: per 32-column
           // chunk, lane r writes row r's 128 bytes into a 32 x 32 staging tile
           // in the 128-byte swizzle (conflict-free 16-byte stores) and one lane
-          // stores the tile; two tiles alternate.  Rows and columns past the
-          // output are clipped by the store.
+          // stores the tile; the staging tiles are used in turn.  Rows and
+          // columns past the output are clipped by the store.
+          if (ti.nkb > 0) {
 #pragma unroll 1
-          for (int c = 0; c < BN / 32; ++c) {
-            float w[32];
-            if (ti.nkb > 0) {
+            for (int c = 0; c < BN / 32; ++c) {
+              float w[32];
               tmem_ld32(tacc + c * 32, w);
-            } else {
-#pragma unroll
-              for (int i = 0; i < 32; ++i) w[i] = 0.f;
+              tma_store_tile32<C::STG_BUFS>(&maps.out, stg_buf(), w, ti.n0 + c * 32,
+                                            ti.m0 + q * 32, ti.e, lane);
             }
-            tma_store_tile32(&maps.out, stg_buf(), w, ti.n0 + c * 32, ti.m0 + q * 32, ti.e, lane);
+          } else {
+            // an expert without rows: every tile of the unit is zero, so one
+            // zeroed staging tile feeds all of the warp's stores (one group)
+            const uint32_t zb = stg_buf();
+            if (lane == 0) bulk_wait_read<C::STG_BUFS - 1>();
+            __syncwarp();
+#pragma unroll
+            for (int j = 0; j < 8; ++j) st_shared_v4(zb + lane * 128 + j * 16, 0.f, 0.f, 0.f, 0.f);
+            fence_async_shared();
+            __syncwarp();
+            if (lane == 0) {
+#pragma unroll 1
+              for (int c = 0; c < BN / 32; ++c) tma_store_3d(&maps.out, zb, ti.n0 + c * 32, ti.m0 + q * 32, ti.e);
+              bulk_commit();
+            }
           }
         } else {
           // routing weight and liveness of this thread's row
