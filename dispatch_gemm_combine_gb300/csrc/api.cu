@@ -429,6 +429,9 @@ moe_status enqueue_gate_up(const moe_shape* s, const void* xp, const void* w_gat
   }
   if (!ok) return MOE_ERR_CUDA;
   m1.a2 = m1.a;
+  // bf16 with concatenated columns tiles tokens on the MMA's N side; short
+  // units use a 32-row box
+  if (es == 2 && !il && !map2d(&m1.a2, es, xp, H, R, H, BK, 32, SW)) return MOE_ERR_CUDA;
   GemmArgs a1 = base_args(s, poff, counts, offsets, perm, topk_w, err);
   a1.out[0] = out_view(aact, I, R, I);
   if (h1) {

@@ -169,6 +169,26 @@ __device__ __forceinline__ void cp_async_wait_all() {
 }
 
 // Make generic-proxy writes to shared memory visible to the async proxy.
+// Named barrier `id` (1..15) over 64 threads, i.e. two whole warps.
+__device__ __forceinline__ void pair_sync(int id) {
+  asm volatile("bar.sync %0, 64;" ::"r"(id) : "memory");
+}
+
+// Named barrier `id` over 64 threads that also returns the AND of `pred`
+// over them.
+__device__ __forceinline__ bool pair_and(int id, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.and.pred q, %2, 64, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(pred ? 1u : 0u), "r"(id)
+      : "memory");
+  return r != 0;
+}
+
 __device__ __forceinline__ void fence_async_shared() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }

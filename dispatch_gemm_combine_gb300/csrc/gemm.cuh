@@ -69,10 +69,16 @@ struct GemmCfg {
   // 256 per pair) and an expert's tokens its N side, in units of up to 256
   // tokens rounded up to 16, so rows that only pad an expert to 128 cost no
   // MMA work.  Used by the bf16 down projection and gate_up dgrad, whose
-  // epilogues write fp32 token rows.
+  // epilogues write fp32 token rows, and by the bf16 gate_up forward with
+  // concatenated [gate | up] columns: a CTA's 128 features are the gate and
+  // the up columns of the same 64 outputs, so the two warps that hold the
+  // gate and the up values of one output pass each other half of a chunk's
+  // tokens through shared memory.
   static constexpr bool SW = SW_;
-  static_assert(!SW || (sizeof(T) == 2 && (MODE == kFwdDown || MODE == kDgradGateUp)),
-                "token-N tiling: bf16 down projection and gate_up dgrad");
+  static_assert(!SW || (sizeof(T) == 2 &&
+                        (MODE == kFwdDown || MODE == kDgradGateUp || MODE == kFwdGateUp)),
+                "token-N tiling: bf16 down projection, gate_up dgrad and gate_up forward");
+  static_assert(!(SW && IL), "token-N tiling of the gate_up forward takes concatenated columns");
   // 2-SM MMA over a CTA pair for every bf16 mode but the down dgrad, whose
   // heavy epilogue would hold up both CTAs (a pair's next MMA waits for both
   // CTAs' epilogues); TF32 keeps independent CTAs
@@ -81,7 +87,7 @@ struct GemmCfg {
   static constexpr int PAIR = CTA2 ? 2 : 1;
   // TF32 operands must be K-major (the fp32 path transposes the others into
   // the workspace first); 16-bit operands may be MN-major.
-  static constexpr bool A_MN = (kWgrad || (SW && MODE == kFwdDown)) && !kTf32;
+  static constexpr bool A_MN = (kWgrad || (SW && (MODE == kFwdDown || MODE == kFwdGateUp))) && !kTf32;
   static constexpr bool B_MN = !SW && (MODE == kFwdGateUp || MODE == kFwdDown || kWgrad) && !kTf32;
   // bf16 weight gradients contract a computed operand (w*a, dH1) that the
   // experts with few effectively weighted rows carry as a bf16 hi/lo pair:
@@ -417,6 +423,38 @@ __device__ __forceinline__ void tma_store_tile32(const CUtensorMap* map, uint32_
   }
 }
 
+// Store n (16 or 32) rows of a tile held by columns as 16-bit values: lane
+// i holds column c0 + i of rows r0 .. r0+n-1 in v[0..n-1].  The per-warp
+// stage holds n rows of 64 bytes (each lane writes its 2-byte value of every
+// row: 64 contiguous bytes per instruction), then every store writes a
+// whole 64-byte row segment (4 lanes x 16 B; a read wavefront of 8 lanes
+// covers two consecutive rows, 128 contiguous bytes).  Rows >= nrows and
+// columns >= o.cols (a multiple of 8) are not written.
+template <typename O, int N>
+__device__ __forceinline__ void store_tile_t16(const OutDesc& o, int r0, int c0, const float* v,
+                                               uint8_t* stage, int lane, int nrows) {
+  O* st = reinterpret_cast<O*>(stage);
+#pragma unroll
+  for (int j = 0; j < N; ++j) {
+    if constexpr (std::is_same<O, __half>::value)
+      st[j * 32 + lane] = __float2half_rn(v[j]);
+    else
+      st[j * 32 + lane] = __float2bfloat16_rn(v[j]);
+  }
+  __syncwarp();
+  O* base = static_cast<O*>(o.ptr);
+  const int c = (lane & 3) * 8;
+  const uint4* s4 = reinterpret_cast<const uint4*>(stage);
+#pragma unroll
+  for (int it = 0; it < N / 8; ++it) {
+    const int r = it * 8 + (lane >> 2);
+    const uint4 val = s4[r * 4 + (lane & 3)];
+    if (r < nrows && c0 + c < o.cols)
+      *reinterpret_cast<uint4*>(base + static_cast<int64_t>(r0 + r) * o.ld + c0 + c) = val;
+  }
+  __syncwarp();
+}
+
 __device__ __forceinline__ float bf16_round(float x) {
   return __bfloat162float(__float2bfloat16_rn(x));
 }
@@ -619,7 +657,12 @@ __global__ void __launch_bounds__(192, 1)
             // A: this CTA's 128 features of the expert's weights (maps.b0);
             // B: this CTA's half of the unit's token rows (maps.a)
             const int f0 = ti.n0 + crank * 128;
-            if constexpr (C::A_MN) {
+            if constexpr (MODE == kFwdGateUp) {
+              // the gate and the up columns of this CTA's 64 outputs
+              const int g0 = ti.n0 + crank * C::CH;
+              load3(sA, &maps.b0, g0, kc, ti.e);
+              load3(sA + C::CHUNK_BYTES, &maps.b1, g0, kc, ti.e);
+            } else if constexpr (C::A_MN) {
 #pragma unroll
               for (int c = 0; c < 128 / C::CH; ++c)
                 load3(sA + c * C::CHUNK_BYTES, &maps.b0, f0 + c * C::CH, kc, ti.e);
@@ -648,22 +691,17 @@ __global__ void __launch_bounds__(192, 1)
           // ---- B: this CTA's BN_CTA columns
           const int nb = ti.n0 + crank * C::BN_CTA;
           if constexpr (MODE == kFwdGateUp && C::B_MN) {
-            // each CTA of the pair holds the gate and the up columns of the
-            // same 64 outputs (n0 + 64*rank ...): tile columns are
-            // [gate 0-63 | up 0-63 | gate 64-127 | up 64-127], so that a half
-            // unit's lanes still see gate and up of one output side by side
+            // bf16 row-grouped gate_up (interleaved columns; concatenated
+            // ones tile tokens on N): each CTA of the pair holds the gate and
+            // the up columns of the same 64 outputs, the 128 consecutive
+            // columns 2*(n0 + 64*rank) ... of the view of all 2I columns, so
+            // that a half unit's lanes still see gate and up of one output
+            // side by side
+            static_assert(C::IL, "bf16 concatenated gate_up columns tile tokens on N");
             static_assert(C::BN_CTA == 2 * C::CH, "gate_up pair tile: one gate and one up chunk per CTA");
-            if constexpr (C::IL) {
-              // interleaved columns (maps.b0 views all 2I): the 128
-              // consecutive columns 2*(n0 + 64*rank) ... hold the gate/up
-              // pairs of this CTA's 64 outputs
-              const int col = 2 * (ti.n0 + crank * C::CH);
-              load3(sB, &maps.b0, col, kc, ti.e);
-              load3(sB + C::CHUNK_BYTES, &maps.b0, col + C::CH, kc, ti.e);
-            } else {
-              load3(sB, &maps.b0, ti.n0 + crank * C::CH, kc, ti.e);
-              load3(sB + C::CHUNK_BYTES, &maps.b1, ti.n0 + crank * C::CH, kc, ti.e);
-            }
+            const int col = 2 * (ti.n0 + crank * C::CH);
+            load3(sB, &maps.b0, col, kc, ti.e);
+            load3(sB + C::CHUNK_BYTES, &maps.b0, col + C::CH, kc, ti.e);
           } else if constexpr (MODE == kFwdGateUp) {
             // K-major (transposed) weights: gate rows then up rows of the tile
             load3(sB, &maps.b0, kc, ti.n0, ti.e);
@@ -836,6 +874,9 @@ __global__ void __launch_bounds__(192, 1)
       int good = 1;
       if (lane == 0) good = mbar_wait(tfull_bar + 8 * acc, acc_phase, tmo);
       good = __shfl_sync(0xffffffffu, good, 0);
+      // the token-N gate_up forward's warp pairs meet at named barriers:
+      // both warps of a pair go on only if both saw the accumulator
+      if constexpr (C::SW && MODE == kFwdGateUp) good = pair_and(1 + (q & 1), good != 0) ? 1 : 0;
       if (!good) {
         if (lane == 0) record_error(args.err, kErrTimeout);
         break;
@@ -851,8 +892,10 @@ __global__ void __launch_bounds__(192, 1)
       // by quarters 0,1 (columns [0, N/2)) and again by 2,3 ([N/2, N))
       const int rq = ti.half ? (q & 1) * 32 : q * 32;
       // token-N tiling: the warp's 32 features (output columns) must exist
+      // (the gate_up forward: the warp's 32 outputs)
       const bool warp_rows =
-          C::SW ? ti.n0 + crank * 128 + q * 32 < args.out[0].cols
+          C::SW ? (MODE == kFwdGateUp ? ti.n0 + crank * C::CH + (q & 1) * 32 < args.out[0].cols
+                                      : ti.n0 + crank * 128 + q * 32 < args.out[0].cols)
                 : C::kWgrad || ti.row0 + rq - __ldg(args.poff + ti.e) < __ldg(args.counts + ti.e);
       if (ti.active && warp_rows) {
         const uint32_t tacc = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * C::ACC_COLS;
@@ -860,7 +903,71 @@ __global__ void __launch_bounds__(192, 1)
         const int orow = ti.row0 + rq;         // first row of this warp's output tiles
         float v[32];
 
-        if constexpr (C::SW) {
+        if constexpr (C::SW && MODE == kFwdGateUp) {
+          // lane = feature, accumulator column = token of the unit.  Warps
+          // q = 0, 1 hold the gate values of outputs o0 + lane, warps q + 2
+          // the up values of the same outputs.  Per 32-token chunk each warp
+          // saves its pre-activations, hands its partner the values of the
+          // half of the tokens the partner finishes (gate warp: tokens
+          // 16-31, up warp: 0-15), and applies the activation to its own
+          // half.
+          const bool up_w = q >= 2;
+          const int o0 = ti.n0 + crank * C::CH + (q & 1) * 32;
+          const int p0 = __ldg(args.poff + ti.e);
+          const int left = min(__ldg(args.counts + ti.e) - (ti.row0 - p0), 256);   // tokens of the unit
+          const int bar_id = 1 + (q & 1);
+          float* mine = reinterpret_cast<float*>(my_epi);
+          const float* peer = reinterpret_cast<const float*>(
+              epi_g + ((warp - 2) ^ 2) * (C::EPI_WARP_BYTES + C::H1_WARP_BYTES));
+          float b = 0.f;
+          if (args.bias && o0 + lane < args.I)
+            b = to_f32(static_cast<const T*>(args.bias)[static_cast<int64_t>(ti.e) * 2 * args.I +
+                                                        (up_w ? args.I : 0) + o0 + lane]);
+          auto run = [&](auto act_c) {
+            constexpr int ACT = decltype(act_c)::value;
+#pragma unroll 1
+            for (int c = 0; c < 8; ++c) {
+              if (c * 32 >= ti.nn) break;   // the same for both warps of the pair
+              const int rows = left - c * 32;   // live tokens from this chunk on (>= 1)
+              tmem_ld32(tacc + c * 32, v);
+              if (args.bias) {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) v[j] += b;
+              }
+              if (args.save_h1) {
+                if (ACT == 1 && args.h1_half) {
+                  // fp16 context (see h1_code_gate)
+                  float hq[32];
+#pragma unroll
+                  for (int j = 0; j < 32; ++j)
+                    hq[j] = up_w ? h1_code_up(v[j], args.limit) : h1_code_gate(v[j], args.limit);
+                  store_tile_t16<__half, 32>(args.out[up_w ? 2 : 1], ti.row0 + c * 32, o0, hq, my_epi,
+                                             lane, rows);
+                } else {
+                  store_tile_t(args.out[up_w ? 2 : 1], ti.row0 + c * 32, o0, v, my_epi, lane, rows,
+                               [](int) { return 1.f; });
+                }
+              }
+#pragma unroll
+              for (int j = 0; j < 16; ++j) mine[j * 32 + lane] = up_w ? v[j] : v[16 + j];
+              pair_sync(bar_id);
+              float a[16];
+#pragma unroll
+              for (int j = 0; j < 16; ++j) {
+                const float o = peer[j * 32 + lane];
+                a[j] = up_w ? act_fwd<ACT>(o, v[16 + j], args.limit, args.alpha)
+                            : act_fwd<ACT>(v[j], o, args.limit, args.alpha);
+              }
+              pair_sync(bar_id);   // the partner has read this warp's half
+              const int h0 = up_w ? 16 : 0;
+              store_tile_t16<T, 16>(args.out[0], ti.row0 + c * 32 + h0, o0, a, my_epi, lane, rows - h0);
+            }
+          };
+          if (args.act == 0)
+            run(std::integral_constant<int, 0>{});
+          else
+            run(std::integral_constant<int, 1>{});
+        } else if constexpr (C::SW) {
           // lane = feature (output column fcol + lane), accumulator column =
           // token of the unit: each 32-token chunk is transposed into token
           // rows; the down projection adds the bias and applies each token's
@@ -969,18 +1076,10 @@ __global__ void __launch_bounds__(192, 1)
                   u[16 + i] = p1[2 * i + 1];
                 }
               } else {
-                int gcol, ucol;   // accumulator columns of this chunk's gate and up values
-                if constexpr (C::CTA2) {
-                  static_assert(BN == 256, "gate_up pair tile layout");
-                  const int tb = ti.half ? 0 : (c >> 1) * 128;
-                  gcol = tb + (c & 1) * 32;
-                  ucol = gcol + 64;
-                } else {
-                  gcol = c * 32;
-                  ucol = BN / 2 + c * 32;
-                }
-                tmem_ld32(tacc + gcol, v);
-                tmem_ld32(tacc + ucol, u);
+                // (TF32, one CTA) accumulator columns [gate | up] of the tile
+                static_assert(!C::CTA2, "pairs take interleaved columns here");
+                tmem_ld32(tacc + c * 32, v);
+                tmem_ld32(tacc + BN / 2 + c * 32, u);
               }
               if (args.bias) {
                 // per-expert gate / up biases of this chunk's outputs
