@@ -74,3 +74,32 @@ def test_pipeline_wait_timeout_unwinds():
     run.check()
     x, i, w, wgu, wd, _ = oracle_inputs(case)
     assert_close("y", y.float().cpu().numpy(), oracle.moe_forward(x, i, w, wgu, wd, ACT_SWIGLU))
+
+
+def test_backward_wait_timeout_unwinds():
+    """The same for the backward's GEMMs (down dgrad, both weight gradients,
+    gate_up dgrad): a 1 ns limit reports MOE_ERR_TIMEOUT, and the next
+    backward with the normal limit matches the oracle."""
+    from dispatch_gemm_combine_gb300 import MOE_ERR_TIMEOUT, MoeError, moe_set_wait_timeout_ns
+    r = Recipe("t", T=1024, H=256, I=256, E=8, k=2, act=ACT_SWIGLU, weight_std="fan_in",
+               routing="softmax_topk_renorm", seed=3)
+    case = to_device(synth.make_case(r))
+    run = _runner(r)
+    run.plan(case.topk_idx)
+    run.forward(case.x, case.topk_idx, case.topk_w, case.w_gate_up, case.w_down)
+    run.check()
+    args = (case.dy, case.x, case.topk_idx, case.topk_w, case.w_gate_up, case.w_down)
+    old = moe_set_wait_timeout_ns(1)
+    try:
+        run.backward(*args)
+        torch.cuda.synchronize()
+    finally:
+        moe_set_wait_timeout_ns(old)
+    with pytest.raises(MoeError) as ei:
+        run.check()
+    assert ei.value.status == MOE_ERR_TIMEOUT
+    dx = run.backward(*args)[0]
+    run.check()
+    x, i, w, wgu, wd, dy = oracle_inputs(case)
+    dx_ref = oracle.moe_backward(dy, x, i, w, wgu, wd, ACT_SWIGLU)[0]
+    assert_close("dx", dx.float().cpu().numpy(), dx_ref)
