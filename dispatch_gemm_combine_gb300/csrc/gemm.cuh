@@ -2,7 +2,8 @@
 // multi-stage shared-memory ring, tcgen05.mma issued by one thread with the
 // fp32 accumulator in tensor memory (double-buffered), and a 4-warp epilogue
 // that reads the accumulator with tcgen05.ld, applies the mode's fused
-// elementwise work and stores 32x32 tiles with coalesced global stores.
+// elementwise work and stores through per-warp shared-memory tiles (row
+// segments of whole sectors, or TMA tensor stores for the weight gradients).
 //
 // bf16 kernels use the 2-SM form of the tensor-core MMA (cta_group::2): a
 // cluster of two CTAs computes a 256 x N tile.  Each CTA loads its own 128
@@ -10,27 +11,29 @@
 // of the even CTA (the leader) issues M=256 MMAs that read both CTAs'
 // tiles, and each CTA's tensor memory receives the accumulator rows of its
 // own A rows.  A CTA therefore receives 2/3 of the operand bytes per FLOP
-// of a single-CTA 128 x N tile: the loads of a k-block (A 16 KB + B 16 KB
-// for N=256) then take less time than its MMAs, which a CTA's TMA delivery
-// rate otherwise cannot match, and the smaller operand traffic leaves the
-// memory system more room for the epilogues' stores.  The bf16 down dgrad,
-// whose epilogue far outweighs its MMAs, and fp32 storage (TF32 products)
-// use independent CTAs and the 1-SM form.
+// of a single-CTA 128 x N tile (A 16 KB + B 16 KB per k-block for N=256),
+// which matters because the operand loads, bounded by the bytes the ring
+// keeps in flight, not the MMAs, set the pace of these kernels.  The bf16
+// down dgrad, whose epilogue far outweighs its MMAs, and fp32 storage (TF32
+// products) use independent CTAs and the 1-SM form.
 //
 // Warp roles: warp 0 = TMA producer, warp 1 = MMA issuer (in the leader)
 // and tensor-memory owner, warps 2..5 = epilogue (warp w reads TMEM lanes
-// 32*(w%4) .. 32*(w%4)+31, i.e. tile rows).  Persistent: each CTA pair walks
-// a static sequence of work units.
+// 32*(w%4) .. 32*(w%4)+31).  Persistent: each CTA pair walks a static
+// sequence of work units.
 //
-// Row-grouped modes (forward and dgrad) tile the tile-padded expert-grouped
-// row space: expert e owns rows [poff[e], poff[e+1]), a multiple of 128, so
-// no M tile straddles two experts; a CTA pair takes two consecutive m-tiles
-// of one expert (the second CTA idles in its epilogue when the expert has an
-// odd number of m-tiles).  Units are ordered (expert, n, m-pair) so the
-// pairs running at the same time share one expert's weight columns in L2.
-// Weight-gradient modes tile the [E, M, N] output (a pair: 256 x N) and
-// contract over the expert's rows, stopping at the MMA step that holds its
-// last row (padding rows are zero-filled).
+// Row-grouped modes (the down dgrad, the interleaved-column gate_up forward
+// and the fp32 forward and dgrads) tile the tile-padded expert-grouped row
+// space: expert e owns rows [poff[e], poff[e+1]), a multiple of 128, so no
+// M tile straddles two experts; a CTA pair takes two consecutive m-tiles of
+// one expert, or one m-tile split 64 + 64 (a half unit) for an expert's odd
+// last tile.  Token-N modes (the other bf16 forward and dgrad GEMMs) put the
+// weights on M and an expert's tokens on N instead, in units of up to 256
+// tokens.  Units are ordered (expert, n, m) so the pairs running at the same
+// time share one expert's weights in L2.  Weight-gradient modes tile the
+// [E, M, N] output (a pair: 256 x N) and contract over the expert's rows,
+// stopping at the MMA step that holds its last row (padding rows are
+// zero-filled).
 //
 // Operand layouts (smem, 128-byte swizzle, what TMA writes):
 //   K-major   box {128 B of K, rows}: 8-row groups 1024 B apart (SBO); the
