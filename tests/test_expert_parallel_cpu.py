@@ -1,4 +1,4 @@
-"""Expert-parallel exchange on two CPU ranks (gloo): every rank's outputs and
+"""Expert-parallel exchange on two and three CPU ranks (gloo): every rank's outputs and
 its experts' weight gradients equal the single-process layer on all ranks'
 tokens.
 
@@ -47,7 +47,7 @@ class OracleOps:
         return src[index[:n].long() // div].clone()
 
     def combine(self, inv, src, T, k, like):
-        return src[inv.long()].reshape(T, k, -1).sum(dim=1)
+        return src[inv.long()].reshape(T, k, src.shape[1]).sum(dim=1)
 
     def expert_forward(self, x_rows, ids, w_rows, E_loc, w_gate_up, w_down, b_gate_up=None,
                        b_down=None):
@@ -147,6 +147,22 @@ def test_expert_parallel_two_ranks_equals_single_process(case_args):
                                                           "d_down")}
         assert all(v <= 1e-12 for v in errs.values()), (r, errs)
     assert out[0]["hi"] == out[1]["lo"] and out[0]["lo"] == 0 and out[1]["hi"] == case_args[3]
+
+
+def test_expert_parallel_three_ranks_one_without_tokens():
+    """Three ranks with uneven expert ranges (2 / 2 / 3 of 7); the middle rank
+    has no tokens of its own but still owns experts that receive rows."""
+    world = 3
+    case_args = ((23, 0, 31), 16, 16, 7, 2, ACT_SWIGLU, "softmax_topk_renorm", False)
+    port = _free_port()
+    out = mp.get_context("spawn").Manager().dict()
+    mp.start_processes(_rank_main, args=(world, port, case_args, out), nprocs=world,
+                       start_method="spawn")
+    for r in range(world):
+        errs = {k: v for k, v in out[r].items() if k in ("y", "dx", "d_topk_w", "d_gate_up",
+                                                          "d_down")}
+        assert all(v <= 1e-12 for v in errs.values()), (r, errs)
+    assert [(out[r]["lo"], out[r]["hi"]) for r in range(world)] == [(0, 2), (2, 4), (4, 7)]
 
 
 def test_expert_ranges_cover_all_experts():
