@@ -33,7 +33,11 @@
  *     on the tensor cores with fp32 accumulation.  dtype MOE_FP32: those
  *     tensors are float32 and the products run as TF32 with fp32
  *     accumulation.  topk weights, d(topk weights) and the weight gradients
- *     are always float32; expert ids are int32.
+ *     are always float32; expert ids are int32.  The fp32 path is meant for
+ *     small correctness cases: every call copies both weight tensors into
+ *     its workspace (transposed for the forward, rounded to TF32 for the
+ *     backward's dgrads) and transposes the gathered rows for the weight
+ *     gradients, so its workspace and traffic grow with E*H*I per call.
  *   - Requirements: T >= 0, 1 <= k <= E <= 1024, T*k < 2^31, H and I
  *     multiples of 8 (16-byte rows for the tensor-memory-access unit),
  *     16-byte aligned pointers.  T = 0 is allowed: outputs with a T extent
