@@ -600,6 +600,8 @@ __global__ void __launch_bounds__(192, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
+    // (one lane issues everything: no warp-wide step on the load path)
+    if (lane == 0) {
     int stage = 0;
     uint32_t phase = 0;
     int64_t issued = 0;
@@ -617,7 +619,6 @@ __global__ void __launch_bounds__(192, 1)
           good = mbar_wait(empty_bar + 8 * stage, phase ^ 1u, tmo);
           if (good && two) good = mbar_wait(empty_bar + 8 * stage2, phase2 ^ 1u, tmo);
         }
-        good = __shfl_sync(0xffffffffu, good, 0);
         if (!good) {
           if (lane == 0) record_error(args.err, kErrTimeout);
           ok = false;
@@ -729,7 +730,6 @@ __global__ void __launch_bounds__(192, 1)
           }
           }
         }
-        __syncwarp();
         // (each slot used counts once: the drain below waits for every use)
         issued += two ? 2 : 1;
         ring_next(stage, phase);
@@ -746,9 +746,11 @@ __global__ void __launch_bounds__(192, 1)
           record_error(args.err, kErrTimeout);
       }
     }
+    }
+    __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (leader) {
+    if (leader && lane == 0) {   // (one lane issues everything)
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
@@ -758,7 +760,6 @@ __global__ void __launch_bounds__(192, 1)
         const TileInfo ti = decode_tile<C::BN_OUT, C::kWgrad, C::PAIR, C::SW>(args, t, C::BK, crank);
         int good = 1;
         if (lane == 0) good = mbar_wait(tempty_bar + 8 * acc, acc_phase ^ 1u, tmo);
-        good = __shfl_sync(0xffffffffu, good, 0);
         if (!good) {
           if (lane == 0) record_error(args.err, kErrTimeout);
           ok = false;
@@ -775,7 +776,6 @@ __global__ void __launch_bounds__(192, 1)
             good = mbar_wait(full_bar + 8 * stage, phase, tmo);
             if (good && two) good = mbar_wait(full_bar + 8 * stage2, phase2, tmo);
           }
-          good = __shfl_sync(0xffffffffu, good, 0);
           if (!good) {
             if (lane == 0) record_error(args.err, kErrTimeout);
             ok = false;
@@ -823,7 +823,6 @@ __global__ void __launch_bounds__(192, 1)
               if (two) tc_commit(empty_bar + 8 * stage2);
             }
           }
-          __syncwarp();
           ring_next(stage, phase);
           if (two) ring_next(stage, phase);
         }
@@ -840,7 +839,6 @@ __global__ void __launch_bounds__(192, 1)
             if constexpr (C::CTA2) mbar_arrive_cluster(mapa_shared(tfull_bar + 8 * acc, 1));
           }
         }
-        __syncwarp();
         if (++acc == 2) {
           acc = 0;
           acc_phase ^= 1u;
@@ -855,8 +853,8 @@ __global__ void __launch_bounds__(192, 1)
         else
           tc_commit(drain_bar);
       }
-      __syncwarp();
     }
+    __syncwarp();
   } else {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;                 // TMEM lane quarter = tile rows q*32..q*32+31
