@@ -602,6 +602,8 @@ __global__ void __launch_bounds__(192, 1)
     // ------------------------------------------------------------ producer
     // (one lane issues everything: no warp-wide step on the load path)
     if (lane == 0) {
+    // the leader's full barriers, which count the bytes of both CTAs
+    const uint32_t full_bar_l = leader_addr(full_bar);
     int stage = 0;
     uint32_t phase = 0;
     int64_t issued = 0;
@@ -626,12 +628,12 @@ __global__ void __launch_bounds__(192, 1)
         }
         if (lane == 0) {
           const uint32_t fb = full_bar + 8 * stage;
-          const uint32_t fbt = leader_addr(fb);
+          const uint32_t fbt = full_bar_l + 8 * stage;
           const uint32_t sA = s_stages + stage * C::STAGE_BYTES;
           const uint32_t sB = sA + C::A_BYTES;
           // the lo part's slot (two-slot k-blocks)
           const uint32_t fb2 = full_bar + 8 * stage2;
-          const uint32_t fbt2 = leader_addr(fb2);
+          const uint32_t fbt2 = full_bar_l + 8 * stage2;
           const uint32_t sA2 = s_stages + stage2 * C::STAGE_BYTES;
           const uint32_t sB2 = sA2 + C::A_BYTES;
           // token-N tiling: a unit of at most 64 tokens (32 rows per CTA)
@@ -768,6 +770,8 @@ __global__ void __launch_bounds__(192, 1)
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * C::ACC_COLS;
         const bool two = C::LO_BYTES > 0 && ti.lo;   // (as in the producer)
+        const uint32_t unit_idesc = C::SW ? make_idesc(C::kTf32, C::A_MN, C::B_MN, 256, ti.nn)
+                                          : (ti.half ? C::IDESC_HALF : C::IDESC);
         for (int kb = 0; kb < ti.nkb; ++kb) {
           int stage2 = stage;
           uint32_t phase2 = phase;
@@ -787,9 +791,7 @@ __global__ void __launch_bounds__(192, 1)
             const uint32_t sB = sA + C::A_BYTES;
             const uint32_t sA2 = s_stages + stage2 * C::STAGE_BYTES;   // lo part (two slots)
             const uint32_t sB2 = sA2 + C::A_BYTES;
-            const uint32_t idesc =
-                C::SW ? make_idesc(C::kTf32, C::A_MN, C::B_MN, 256, ti.nn)
-                      : (ti.half ? C::IDESC_HALF : C::IDESC);
+            const uint32_t idesc = unit_idesc;
             auto mma = [&](uint64_t ad, uint64_t bd, uint32_t accum) {
               if constexpr (C::CTA2)
                 tc_mma2(d_tmem, ad, bd, idesc, accum);
