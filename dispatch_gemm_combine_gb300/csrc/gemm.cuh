@@ -118,6 +118,11 @@ struct GemmCfg {
   // dgrad measured within 2% of the shared-memory transposes, so those keep
   // the register paths.
   static constexpr bool TMA_OUT = kWgrad;
+  // The producer and the MMA issuer run on one lane (no warp-wide step per
+  // k-block), except in the weight gradients, which measured faster with
+  // the whole warp stepping through each k-block (their fp32 stores, not
+  // the loads, set their pace).
+  static constexpr bool kOneLane = !kWgrad;
   static constexpr int H1_WARP_BYTES = (MODE == kDgradDown) ? 32 * 68 * 4 : 0;
   static constexpr int BAR_BYTES = (2 * STAGES + 5) * 8 + 16;
   // TMA_OUT: each epilogue warp stages its stores in STG_BUFS 32 x 32 fp32
@@ -600,8 +605,9 @@ __global__ void __launch_bounds__(192, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    // (one lane issues everything: no warp-wide step on the load path)
-    if (lane == 0) {
+    // (one lane issues everything unless the mode keeps the whole warp in
+    // step, see GemmCfg::kOneLane)
+    if (!C::kOneLane || lane == 0) {
     // the leader's full barriers, which count the bytes of both CTAs
     const uint32_t full_bar_l = leader_addr(full_bar);
     int stage = 0;
@@ -621,6 +627,7 @@ __global__ void __launch_bounds__(192, 1)
           good = mbar_wait(empty_bar + 8 * stage, phase ^ 1u, tmo);
           if (good && two) good = mbar_wait(empty_bar + 8 * stage2, phase2 ^ 1u, tmo);
         }
+        if constexpr (!C::kOneLane) good = __shfl_sync(0xffffffffu, good, 0);
         if (!good) {
           if (lane == 0) record_error(args.err, kErrTimeout);
           ok = false;
@@ -732,6 +739,7 @@ __global__ void __launch_bounds__(192, 1)
           }
           }
         }
+        if constexpr (!C::kOneLane) __syncwarp();
         // (each slot used counts once: the drain below waits for every use)
         issued += two ? 2 : 1;
         ring_next(stage, phase);
@@ -752,7 +760,7 @@ __global__ void __launch_bounds__(192, 1)
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (leader && lane == 0) {   // (one lane issues everything)
+    if (leader && (!C::kOneLane || lane == 0)) {   // (one lane, see GemmCfg::kOneLane)
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
@@ -762,6 +770,7 @@ __global__ void __launch_bounds__(192, 1)
         const TileInfo ti = decode_tile<C::BN_OUT, C::kWgrad, C::PAIR, C::SW>(args, t, C::BK, crank);
         int good = 1;
         if (lane == 0) good = mbar_wait(tempty_bar + 8 * acc, acc_phase ^ 1u, tmo);
+        if constexpr (!C::kOneLane) good = __shfl_sync(0xffffffffu, good, 0);
         if (!good) {
           if (lane == 0) record_error(args.err, kErrTimeout);
           ok = false;
@@ -780,6 +789,7 @@ __global__ void __launch_bounds__(192, 1)
             good = mbar_wait(full_bar + 8 * stage, phase, tmo);
             if (good && two) good = mbar_wait(full_bar + 8 * stage2, phase2, tmo);
           }
+          if constexpr (!C::kOneLane) good = __shfl_sync(0xffffffffu, good, 0);
           if (!good) {
             if (lane == 0) record_error(args.err, kErrTimeout);
             ok = false;
@@ -825,6 +835,7 @@ __global__ void __launch_bounds__(192, 1)
               if (two) tc_commit(empty_bar + 8 * stage2);
             }
           }
+          if constexpr (!C::kOneLane) __syncwarp();
           ring_next(stage, phase);
           if (two) ring_next(stage, phase);
         }
@@ -841,6 +852,7 @@ __global__ void __launch_bounds__(192, 1)
             if constexpr (C::CTA2) mbar_arrive_cluster(mapa_shared(tfull_bar + 8 * acc, 1));
           }
         }
+        if constexpr (!C::kOneLane) __syncwarp();
         if (++acc == 2) {
           acc = 0;
           acc_phase ^= 1u;
