@@ -430,6 +430,8 @@ def main():
     ap.add_argument("--tokens", type=int, default=None,
                     help="run the workload at this many tokens (the load-imbalance sweep's T "
                          "values); the bench line itself uses the workload's own T")
+    ap.add_argument("--gate-up-layout", choices=["concat", "interleaved"], default="concat",
+                    help="column layout of w_gate_up (the same random weights either way)")
     ap.add_argument("--experts", type=int, default=None,
                     help="profiling case: use this many experts and scale the tokens so each "
                          "expert keeps the workload's rows (not a bench line)")
@@ -462,7 +464,8 @@ def main():
         r = r.scaled(E=args.experts, T=max(1, r.T * args.experts // r.E))
     case = synth.make_case(r, device="cuda")
     dt = MOE_BF16 if r.dtype == "bf16" else MOE_FP32
-    run = LayerRunner(r.T, r.H, r.I, r.E, r.k, r.act, dt, r.limit, r.alpha)
+    layout = 1 if args.gate_up_layout == "interleaved" else 0
+    run = LayerRunner(r.T, r.H, r.I, r.E, r.k, r.act, dt, r.limit, r.alpha, gate_up_layout=layout)
     stream = torch.cuda.current_stream()
 
     def step():
@@ -546,7 +549,8 @@ def main():
     # running step uses.  Every step still moves its whole inputs and results
     # across the host link; the timed region runs from the first input copy to
     # the last result copy.
-    runs = [run, LayerRunner(r.T, r.H, r.I, r.E, r.k, r.act, dt, r.limit, r.alpha)]
+    runs = [run, LayerRunner(r.T, r.H, r.I, r.E, r.k, r.act, dt, r.limit, r.alpha,
+                             gate_up_layout=layout)]
     h_in = {n: getattr(case, n).cpu().pin_memory() for n in ("x", "topk_idx", "topk_w", "dy")}
     d_in = [{n: torch.empty_like(getattr(case, n)) for n in h_in} for _ in runs]
     h_out = [{"y": torch.empty(run.y.shape, dtype=run.y.dtype).pin_memory(),
@@ -618,7 +622,8 @@ def main():
     y_ref = run.forward(case.x, case.topk_idx, case.topk_w, case.w_gate_up, case.w_down).clone()
     dx_ref = run.backward(case.dy, case.x, case.topk_idx, case.topk_w, case.w_gate_up,
                           case.w_down)[0].clone()
-    ep = ExpertParallelMoE(r.E, r.k, CudaOps(r.H, r.I, r.act, dt, r.limit, r.alpha))
+    ep = ExpertParallelMoE(r.E, r.k, CudaOps(r.H, r.I, r.act, dt, r.limit, r.alpha,
+                                             gate_up_layout=layout))
 
     def ep_step():
         ep.forward(case.x, case.topk_idx, case.topk_w, case.w_gate_up, case.w_down)
@@ -708,6 +713,7 @@ def main():
         "config": {"workload": workload_name(args.workload, r),
                    "T": r.T, "H": r.H, "I": r.I, "E": r.E, "k": r.k, "seed": r.seed,
                    "parallelism": "replicas" if world > 1 else "single GPU",
+                   "gate_up_layout": args.gate_up_layout,
                    "l2": "no flush: %.1f GB of expert weights per step exceed the 129 MB L2"
                          % (r.E * 3 * r.H * r.I * case.w_down.element_size() / 1e9)},
         "step_ms": step_stats,
