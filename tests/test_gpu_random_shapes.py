@@ -1,4 +1,5 @@
-"""GPU parity on seeded random shapes: H and I any multiple of 8 from 8 up
+"""GPU parity on seeded random shapes (the second test adds a random gate_up
+layout and a random choice of biases): H and I any multiple of 8 from 8 up
 (below one 64-element k-block, below one 128-feature tile, ragged against
 both), 1 to 40 experts, k up to 8, 1 to 700 tokens, both activations, both
 storage dtypes and all four routing kinds.  Every output against the fp64
@@ -75,3 +76,58 @@ def test_random_shape_parity(i, T, H, I, E, k, act, dtype, routing):
         assert_close("d_gate[%d]" % e, got[:, :I], dgu_ref[e][:, :I])
         assert_close("d_up[%d]" % e, got[:, I:], dgu_ref[e][:, I:])
         assert_close("d_down[%d]" % e, dwd[e].double().cpu().numpy(), dd_ref[e])
+
+
+def _layout_bias_cases(n=24, seed=2025):
+    """The first n random shapes again, each with a random gate_up layout and
+    a random choice of biases (none, gate_up, down, both)."""
+    g = np.random.default_rng(seed)
+    return [c + (int(g.integers(0, 2)), ("none", "gate_up", "down", "both")[int(g.integers(0, 4))])
+            for c in _cases()[:n]]
+
+
+@pytest.mark.parametrize("i,T,H,I,E,k,act,dtype,routing,layout,biases", _layout_bias_cases())
+def test_random_shape_layout_and_bias_parity(i, T, H, I, E, k, act, dtype, routing, layout,
+                                             biases):
+    from dispatch_gemm_combine_gb300 import MOE_BF16, MOE_FP32
+    from dispatch_gemm_combine_gb300.runner import LayerRunner
+    from tests.helpers import f64
+    r = Recipe("rand", T=T, H=H, I=I, E=E, k=k, act=act, dtype=dtype, weight_std="fan_in",
+               routing=routing, seed=7000 + i)
+    case = synth.make_case(r)
+    use_gu, use_d = biases in ("both", "gate_up"), biases in ("both", "down")
+    bgu_t, bd_t = synth.make_biases(r) if biases != "none" else (None, None)
+    x, idx, w, wgu_l, wd, dy = oracle_inputs(case)
+    wgu = oracle.gate_up_concatenated(wgu_l, layout)
+    bgu = oracle.gate_up_concatenated(f64(bgu_t), layout) if use_gu else None
+    bd = f64(bd_t) if use_d else None
+    d = to_device(case)
+    bkw = dict(b_gate_up=bgu_t.cuda() if use_gu else None, b_down=bd_t.cuda() if use_d else None)
+    run = LayerRunner(T, H, I, E, k, act, MOE_FP32 if dtype == "fp32" else MOE_BF16, r.limit,
+                      r.alpha, gate_up_layout=layout)
+    run.plan(d.topk_idx)
+    y = run.forward(d.x, d.topk_idx, d.topk_w, d.w_gate_up, d.w_down, **bkw).clone()
+    grads = [t.clone() for t in run.backward(d.dy, d.x, d.topk_idx, d.topk_w, d.w_gate_up,
+                                             d.w_down, **bkw)]
+    torch.cuda.synchronize()
+    run.check()
+    okw = dict(b_gate_up=bgu, b_down=bd)
+    y_ref = oracle.moe_forward(x, idx, w, wgu, wd, act, **okw)
+    ref = oracle.moe_backward(dy, x, idx, w, wgu, wd, act, **okw)
+    check = assert_close_bf16_output if dtype == "bf16" else assert_close
+    check("y", y.double().cpu().numpy(), y_ref)
+    check("dx", grads[0].double().cpu().numpy(), ref[0])
+    assert_dw_close(grads[1].cpu().numpy(), ref[1])
+    counts = np.bincount(idx.reshape(-1), minlength=E)
+    for e in range(E):
+        got = oracle.gate_up_concatenated(grads[2][e].double().cpu().numpy(), layout)
+        if counts[e] == 0:
+            assert not got.any() and torch.all(grads[3][e] == 0), e
+        else:
+            assert_close("d_gate[%d]" % e, got[:, :I], ref[2][e][:, :I])
+            assert_close("d_up[%d]" % e, got[:, I:], ref[2][e][:, I:])
+            assert_close("d_down[%d]" % e, grads[3][e].double().cpu().numpy(), ref[3][e])
+    if biases != "none":
+        dbgu = oracle.gate_up_concatenated(grads[4].double().cpu().numpy(), layout)
+        assert_close("db_gate_up", dbgu, ref[4])
+        assert_close("db_down", grads[5].double().cpu().numpy(), ref[5])
