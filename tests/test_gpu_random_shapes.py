@@ -6,7 +6,8 @@ storage dtypes and all four routing kinds.  Every output against the fp64
 oracle: y and dx (bf16 outputs: relative Frobenius and max abs <= 3e-2 rms
 plus one bf16 step of the reference element), d(topk w), and every expert's
 gate, up and down weight gradients, with exact zeros for experts without a
-token."""
+token; the backward that recomputes the saved context must match the one
+that reads it bit for bit."""
 
 import numpy as np
 import pytest
@@ -55,8 +56,12 @@ def test_random_shape_parity(i, T, H, I, E, k, act, dtype, routing):
     y = run.forward(d.x, d.topk_idx, d.topk_w, d.w_gate_up, d.w_down).clone()
     dx, dtw, dwgu, dwd = [t.clone() for t in run.backward(d.dy, d.x, d.topk_idx, d.topk_w,
                                                           d.w_gate_up, d.w_down)]
+    # the backward without the saved context recomputes it: bit for bit the same
+    again = run.backward(d.dy, d.x, d.topk_idx, d.topk_w, d.w_gate_up, d.w_down, recompute=True)
     torch.cuda.synchronize()
     run.check()
+    for a, b in zip((dx, dtw, dwgu, dwd), again):
+        assert torch.equal(a, b)
     x, idx, w, wgu, wd, dy = oracle_inputs(case)
     y_ref = oracle.moe_forward(x, idx, w, wgu, wd, act)
     dx_ref, dw_ref, dgu_ref, dd_ref = oracle.moe_backward(dy, x, idx, w, wgu, wd, act)
