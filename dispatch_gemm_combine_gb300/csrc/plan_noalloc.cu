@@ -35,7 +35,7 @@ static __device__ __align__(256) int g_plan_scratch[kScratchInts];
 // Device address of g_plan_scratch.  In host code the symbol names a
 // host-side stand-in, never the device array, so the address is resolved
 // with cudaGetSymbolAddress, with the device current.  It is resolved once
-// per device context: the cache remembers the driver's unique id of the
+// per device context: the cache remembers the CUDA driver's unique id of the
 // context it was resolved in, and a call that finds another context current
 // (after cudaDeviceReset, the module and its array are loaded anew) resolves
 // it again instead of using a stale address.
